@@ -1,0 +1,11 @@
+"""fp64 CPU oracle for exact attention -- test infrastructure only.
+
+Imported by the tests, the smoke check and the benchmark's CPU-baseline leg;
+never by the library.  See ``oracle/attention.py`` for what it computes and
+which passages each function follows.
+"""
+from .attention import (backward, bf16_bits_to_f64, causal_visible, e4m3_to_f64,
+                        forward, head_backward, head_forward, scores, softmax_rows)
+
+__all__ = ["backward", "bf16_bits_to_f64", "causal_visible", "e4m3_to_f64",
+           "forward", "head_backward", "head_forward", "scores", "softmax_rows"]
