@@ -1,0 +1,350 @@
+// C ABI of libattn_sm103a.so: argument validation, TMA tensor maps, launch
+// sequencing and the device error word.  The declarations and their contract
+// are in include/attn_sm103a.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn_sm103a.h"
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+// Device error word: [0] error bits, [1] id of the first wait that gave up.
+__device__ unsigned int g_err_word[2];
+
+constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
+unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool probed = false;
+    bool supported = false;
+    unsigned int* err = nullptr;  // device address of g_err_word on this device
+};
+DeviceState g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Per-device setup, done once with that device current: check the
+// architecture and look up the device address of the error word.
+attn_status device_state(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState& s = g_dev[dev];
+    if (!s.probed) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        s.supported = (major == 10 && minor == 3);
+        void* p = nullptr;
+        if (s.supported) {
+            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return ATTN_ERR_CUDA;
+        }
+        s.err = static_cast<unsigned int*>(p);
+        s.probed = true;
+    }
+    if (!s.supported) return ATTN_ERR_UNSUPPORTED;
+    *out = &s;
+    return ATTN_OK;
+}
+
+DevStatus dev_status(const DeviceState* s) {
+    DevStatus st;
+    st.word = s->err;
+    st.wait_limit_ns = g_wait_limit_ns;
+    return st;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point, so that the
+// library has no link-time dependency on libcuda.
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = []() -> EncodeTiledFn {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// 3-D view {d, N, B*H} of a dense [B, H, N, d] tensor; box {inner, 128, 1},
+// 128-byte swizzle, out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int BH) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t eb = fp8 ? 1 : 2;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {d * eb, static_cast<cuuint64_t>(N) * d * eb};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 128u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+               const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+constexpr long long kMaxElems = (1ll << 40);  // keeps every byte offset well inside 64 bits
+
+attn_status check_sizes(int B, int H, int N, int d, float scale, int causal) {
+    if (B < 1 || H < 1 || N < 1) return ATTN_ERR_INVALID;
+    if (!(scale > 0.f) || !std::isfinite(scale)) return ATTN_ERR_INVALID;
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (d <= 0) return ATTN_ERR_INVALID;
+    if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+    const long long bh = static_cast<long long>(B) * H;
+    if (bh > (1ll << 31) - 1) return ATTN_ERR_INVALID;
+    if (bh * N * d > kMaxElems) return ATTN_ERR_INVALID;
+    const long long ctas = bh * ((N + 2 * kTile - 1) / (2 * kTile));
+    const long long ctas_bwd = bh * ((N + kTile - 1) / kTile);
+    if (ctas > 0x7fffffffll || ctas_bwd > 0x7fffffffll) return ATTN_ERR_INVALID;
+    return ATTN_OK;
+}
+
+long long npad(int N) { return (static_cast<long long>(N) + kTile - 1) / kTile * kTile; }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct BwdLayout {
+    size_t dq_acc, lse2, dsum, total;
+};
+
+BwdLayout bwd_layout(int B, int H, int N, int d) {
+    const size_t rows = static_cast<size_t>(B) * H * npad(N);
+    BwdLayout L;
+    L.dq_acc = 0;
+    L.lse2 = round256(rows * d * sizeof(float));
+    L.dsum = L.lse2 + round256(rows * sizeof(float));
+    L.total = L.dsum + round256(rows * sizeof(float));
+    return L;
+}
+
+__global__ void wait_selftest_kernel(DevStatus st) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);  // nothing ever arrives on it
+        abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x < 32) {
+        wait_warp(b, 0, &abort_flag, st, 0x901);
+    } else if (threadIdx.x == 32) {
+        wait_one(b, 0, &abort_flag, st, 0x902);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 64, 0, stream>>>(st);
+    return cudaGetLastError();
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, float scale, int causal, attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_INVALID;
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, BH) ||
+        !make_map(&tv, v, false, d, N, BH))
+        return ATTN_ERR_CUDA;
+    FwdParams p;
+    p.o = o;
+    p.lse = lse;
+    p.N = N;
+    p.BH = BH;
+    p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
+    p.causal = causal;
+    p.cs = scale * 1.44269504088896340736f;
+    p.out_scale = 1.f;
+    p.st = dev_status(ds);
+    return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float sq, float sk, float sv,
+                         void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                         attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    for (float s : {sq, sk, sv})
+        if (!(s > 0.f) || !std::isfinite(s)) return ATTN_ERR_INVALID;
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_INVALID;
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+    const int BH = B * H;
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, q8, true, d, N, BH) || !make_map(&tk, k8, true, d, N, BH) ||
+        !make_map(&tv, v8, true, d, N, BH))
+        return ATTN_ERR_CUDA;
+    FwdParams p;
+    p.o = o;
+    p.lse = lse;
+    p.N = N;
+    p.BH = BH;
+    p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
+    p.causal = causal;
+    p.cs = scale * sq * sk * 1.44269504088896340736f;
+    p.out_scale = sv;
+    p.st = dev_status(ds);
+    return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
+    return bwd_layout(B, H, N, d).total;
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                     int N, int d, float scale, int causal, attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (!aligned16(p)) return ATTN_ERR_INVALID;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_INVALID;
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+    const int BH = B * H;
+    const BwdLayout L = bwd_layout(B, H, N, d);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    float* dsum = reinterpret_cast<float*>(ws + L.dsum);
+    const int Np = static_cast<int>(npad(N));
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, BH) ||
+        !make_map(&tv, v, false, d, N, BH) || !make_map(&tdo, dout, false, d, N, BH))
+        return ATTN_ERR_CUDA;
+
+    BwdPreParams pp;
+    pp.o = o;
+    pp.dout = dout;
+    pp.lse = lse;
+    pp.dq_acc = dq_acc;
+    pp.lse2 = lse2;
+    pp.dsum = dsum;
+    pp.N = N;
+    pp.Npad = Np;
+    pp.BH = BH;
+    pp.D = d;
+    if (launch_bwd_pre(pp, st) != cudaSuccess) return ATTN_ERR_CUDA;
+
+    BwdParams bp;
+    bp.lse2 = lse2;
+    bp.dsum = dsum;
+    bp.dq_acc = dq_acc;
+    bp.dk = dk;
+    bp.dv = dv;
+    bp.N = N;
+    bp.Npad = Np;
+    bp.BH = BH;
+    bp.n_kv = (N + kTile - 1) / kTile;
+    bp.causal = causal;
+    bp.cs = scale * 1.44269504088896340736f;
+    bp.scale = scale;
+    bp.st = dev_status(ds);
+    if (launch_bwd_main(d, tq, tk, tv, tdo, bp, st) != cudaSuccess) return ATTN_ERR_CUDA;
+
+    DqConvertParams cp;
+    cp.dq_acc = dq_acc;
+    cp.dq = dq;
+    cp.N = N;
+    cp.Npad = Np;
+    cp.BH = BH;
+    cp.D = d;
+    cp.scale = scale;
+    if (launch_dq_convert(cp, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}
+
+attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site) {
+    if (site) *site = 0;
+    DeviceState* ds = nullptr;
+    attn_status rc = device_state(&ds);
+    if (rc != ATTN_OK) return rc;
+    if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    unsigned int host[2] = {0, 0};
+    const unsigned int zero[2] = {0, 0};
+    if (cudaMemcpy(host, ds->err, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(ds->err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (site) *site = host[1];
+    return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
+}
+
+void attn_set_wait_limit_ns(unsigned long long ns) {
+    g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs;
+}
+
+attn_status attn_selftest_wait_timeout(attn_stream_t stream) {
+    DeviceState* ds = nullptr;
+    attn_status rc = device_state(&ds);
+    if (rc != ATTN_OK) return rc;
+    return launch_wait_selftest(dev_status(ds), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+const char* attn_status_string(attn_status s) {
+    switch (s) {
+        case ATTN_OK: return "ATTN_OK";
+        case ATTN_ERR_INVALID: return "ATTN_ERR_INVALID";
+        case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+        case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+        case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    }
+    return "ATTN_ERR_UNKNOWN";
+}
+
+int attn_kernel_smem_bytes(int which, int d) {
+    if (which == 0) return fwd_smem_bytes(d, false);
+    if (which == 1) return fwd_smem_bytes(d, true);
+    if (which == 2) return bwd_smem_bytes(d);
+    return 0;
+}
+
+}  // extern "C"

@@ -1,0 +1,472 @@
+// Backward exact attention on sm_103a.  Three launches on one stream:
+//
+//  1. bwd_pre     D_i = sum_k dO_ik O_ik (equal to sum_j P_ij dP_ij), LSE in
+//                 log2 units, zeroed fp32 dQ accumulator.
+//  2. bwd_main    one CTA per (batch*head, 128-key tile j); loops over query
+//                 tiles i, regenerating P from Q, K and the saved log-sum-exp
+//                 (FlashAttention item 58: backward recomputes score tiles from
+//                 inputs and normalisation statistics):
+//                     S^T  = K Q_i^T            P^T = 2^(S^T*cs - LSE2)
+//                     dP^T = V dO_i^T           dS^T = P^T (dP^T - D)
+//                     dV  += P^T dO_i           dK  += dS^T Q_i
+//                     dQ_i += dS K   (fp32 reductions into the accumulator)
+//                 The dQ reductions are done by a dedicated writer warpgroup,
+//                 the role the FlashAttention-3 digest (section 1) gives its
+//                 dQ-writer warp.
+//  3. dq_convert  dQ = bf16(scale * accumulator)  (the second, combining
+//                 kernel of a split reduction, CUTLASS split-K item).
+//
+// bwd_main warp roles (320 threads):
+//   warps 0-3  compute: P^T, dS^T (one thread per key row); dK/dV epilogue
+//   warps 4-7  dQ writer: tensor memory -> red.global.add.v4.f32
+//   warp 8     TMA producer: K_j, V_j once; Q_i, dO_i, LSE2_i, D_i per step
+//   warp 9     MMA issuer
+// Tensor memory (lane = key row for S^T, dP^T, dV, dK; lane = query row for dQ):
+//   [0,128)    S^T (fp32), then P^T packed bf16 in its first 64 columns
+//   [128,256)  dP^T (fp32); once read, reused for the dQ_i tile
+//   [256,256+D)      dV accumulator
+//   [256+D,256+2D)   dK accumulator
+// Shared memory: K, V, two stages of (Q, dO, LSE2, D), and dS^T (bf16,
+// 128-byte swizzle), which serves as the K-major A operand of dK and, read
+// MN-major, as the A operand dS of dQ.
+#include <cuda_runtime.h>
+
+#include "attn_internal.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr float kLog2e = 1.44269504088896340736f;
+
+template <int D>
+struct BwdTraits {
+    static constexpr int NBLK = D / 64;
+    static constexpr int BLK_BYTES = kTile * 128;
+    static constexpr int TILE_BYTES = kTile * D * 2;
+    static constexpr int DS_BYTES = kTile * kTile * 2;
+    static constexpr int STAGES = 2;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + TILE_BYTES;
+    static constexpr int OFF_Q = OFF_V + TILE_BYTES;                 // + stage * TILE_BYTES
+    static constexpr int OFF_DO = OFF_Q + STAGES * TILE_BYTES;       // + stage * TILE_BYTES
+    static constexpr int OFF_DS = OFF_DO + STAGES * TILE_BYTES;
+    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;                // LSE2[s], D[s]: 512 B each
+    static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * 512;
+    // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full, p_full, dq_full, dq_empty, dkv_full, done
+    static constexpr int NBARS = 1 + 2 * STAGES + 6;
+    static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
+    static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, kTile, false, false);
+    static constexpr uint32_t IDESC_DV = make_idesc(kFmtBF16, kTile, D, false, true);
+    static constexpr uint32_t IDESC_DQ = make_idesc(kFmtBF16, kTile, D, true, true);
+    static constexpr uint32_t IDESC_DK = make_idesc(kFmtBF16, kTile, D, false, true);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+enum : uint32_t {
+    SITE_KV = 0x201, SITE_QDO_EMPTY = 0x202, SITE_QDO_FULL = 0x203, SITE_DQ_EMPTY = 0x204,
+    SITE_P_FULL = 0x205, SITE_S_FULL = 0x206, SITE_DQ_FULL = 0x207, SITE_DKV = 0x208,
+    SITE_DRAIN = 0x209,
+};
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// ---------------------------------------------------------------------------
+// 1. preprocess: one warp per (head, row) of the padded row range
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
+    const int lane = threadIdx.x & 31;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const long long rows = static_cast<long long>(p.BH) * p.Npad;
+    const int epl = p.D / 32;  // bf16 elements per lane (2 or 4)
+    for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        const int bh = static_cast<int>(r / p.Npad);
+        const int n = static_cast<int>(r % p.Npad);
+        float acc = 0.f;
+        if (n < p.N) {
+            const size_t base = (static_cast<size_t>(bh) * p.N + n) * p.D + lane * epl;
+            const uint16_t* o16 = static_cast<const uint16_t*>(p.o) + base;
+            const uint16_t* d16 = static_cast<const uint16_t*>(p.dout) + base;
+            if (epl == 4) {
+                const uint2 a = *reinterpret_cast<const uint2*>(o16);
+                const uint2 b = *reinterpret_cast<const uint2*>(d16);
+                acc = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x) +
+                      bf16lo(a.y) * bf16lo(b.y) + bf16hi(a.y) * bf16hi(b.y);
+            } else {
+                const uint32_t a = *reinterpret_cast<const uint32_t*>(o16);
+                const uint32_t b = *reinterpret_cast<const uint32_t*>(d16);
+                acc = bf16lo(a) * bf16lo(b) + bf16hi(a) * bf16hi(b);
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) {
+            const size_t v = static_cast<size_t>(bh) * p.Npad + n;
+            p.dsum[v] = acc;
+            p.lse2[v] = n < p.N ? p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e : INFINITY;
+        }
+        float4* z = reinterpret_cast<float4*>(p.dq_acc + r * p.D);
+        for (int c = lane; c < p.D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dQ conversion: 8 elements per thread
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
+    const long long total = static_cast<long long>(p.BH) * p.N * (p.D / 8);
+    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
+         t += stride) {
+        const long long row = t / (p.D / 8);  // bh * N + n
+        const int c8 = static_cast<int>(t % (p.D / 8));
+        const int bh = static_cast<int>(row / p.N);
+        const int n = static_cast<int>(row % p.N);
+        const float4* src = reinterpret_cast<const float4*>(
+            p.dq_acc + (static_cast<size_t>(bh) * p.Npad + n) * p.D + c8 * 8);
+        const float4 a = src[0], b = src[1];
+        const float s = p.scale;
+        uint32_t w0 = pack_bf16x2(a.x * s, a.y * s), w1 = pack_bf16x2(a.z * s, a.w * s);
+        uint32_t w2 = pack_bf16x2(b.x * s, b.y * s), w3 = pack_bf16x2(b.z * s, b.w * s);
+        st_global_v4(static_cast<uint16_t*>(p.dq) + row * p.D + c8 * 8, w0, w1, w2, w3);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 2. main kernel
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(320, 1)
+    bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const BwdParams prm) {
+    using T = BwdTraits<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + T::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t b_kv = bar0;
+    auto b_qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto b_qdo_empty = [&](int s) { return bar0 + 8u * (1 + T::STAGES + s); };
+    const uint32_t b_s_full = bar0 + 8u * (1 + 2 * T::STAGES);
+    const uint32_t b_p_full = b_s_full + 8u;
+    const uint32_t b_dq_full = b_s_full + 16u;
+    const uint32_t b_dq_empty = b_s_full + 24u;
+    const uint32_t b_dkv_full = b_s_full + 32u;
+    const uint32_t b_done = b_s_full + 40u;
+
+    if ((sbase & 1023u) != 0) {
+        if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FF);
+        return;
+    }
+
+    const int N = prm.N;
+    const int bh = blockIdx.x % prm.BH;
+    const int j = static_cast<int>(blockIdx.x / prm.BH);  // key tile; low j first (longest causal loops)
+    const int n_q_total = (N + kTile - 1) / kTile;
+    const int i0 = prm.causal ? j : 0;
+    const int n_steps = n_q_total - i0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv, 1);
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(b_qdo_full(s), 1);
+            mbar_init(b_qdo_empty(s), 1);
+        }
+        mbar_init(b_s_full, 1);
+        mbar_init(b_p_full, 4);
+        mbar_init(b_dq_full, 1);
+        mbar_init(b_dq_empty, 4);
+        mbar_init(b_dkv_full, 1);
+        mbar_init(b_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 9) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == 8 && lane == 0) {
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+        tma_prefetch_map(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const float* lse2_g = prm.lse2 + static_cast<size_t>(bh) * prm.Npad;
+    const float* dsum_g = prm.dsum + static_cast<size_t>(bh) * prm.Npad;
+
+    if (warp == 8) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
+            for (int blk = 0; blk < T::NBLK; ++blk) {
+                tma_load_3d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile, bh);
+                tma_load_3d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile, bh);
+            }
+            int t = 0;
+            for (; t < n_steps; ++t) {
+                const int s = t % T::STAGES;
+                const int i = i0 + t;
+                if (t >= T::STAGES &&
+                    !wait_one(b_qdo_empty(s), ((t / T::STAGES) - 1) & 1, abort_flag, prm.st,
+                              SITE_QDO_EMPTY))
+                    break;
+                const uint32_t bf = b_qdo_full(s);
+                mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
+                for (int blk = 0; blk < T::NBLK; ++blk) {
+                    tma_load_3d(sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_q, bf,
+                                blk * 64, i * kTile, bh);
+                    tma_load_3d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
+                                blk * 64, i * kTile, bh);
+                }
+                bulk_load(sbase + T::OFF_VEC + s * 1024, lse2_g + i * kTile, 512, bf);
+                bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, dsum_g + i * kTile, 512, bf);
+            }
+            wait_drain(b_kv, 0, prm.st, SITE_DRAIN);
+            const int first = t > T::STAGES ? t - T::STAGES : 0;
+            for (int u = first; u < t; ++u)
+                wait_drain(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, prm.st, SITE_DRAIN);
+        }
+    } else if (warp == 9) {
+        // ================= MMA issuer =================
+        if (lane == 0) {
+            const uint32_t tS = tmem + T::COL_S, tDP = tmem + T::COL_DP;
+            const uint32_t tDV = tmem + T::COL_DV, tDK = tmem + T::COL_DK;
+            const uint32_t sK = sbase + T::OFF_K, sV = sbase + T::OFF_V, sDS = sbase + T::OFF_DS;
+            // K-major operand, 16 bf16 (32 bytes) of K per instruction.
+            auto kmaj = [](uint32_t base, int kk) {
+                return sw128_desc(base + (kk >> 2) * T::BLK_BYTES + (kk & 3) * 32, 16, 1024);
+            };
+            // MN-major operand: rows are the reduction index, 16 rows per instruction.
+            auto mnmaj = [](uint32_t base, int kk) {
+                return sw128_desc(base + kk * 16 * 128, T::BLK_BYTES, 1024);
+            };
+            auto run = [&]() -> bool {
+                if (!wait_one(b_kv, 0, abort_flag, prm.st, SITE_KV)) return false;
+                for (int t = 0; t < n_steps; ++t) {
+                    const int s = t % T::STAGES;
+                    const uint32_t sQ = sbase + T::OFF_Q + s * T::TILE_BYTES;
+                    const uint32_t sDO = sbase + T::OFF_DO + s * T::TILE_BYTES;
+                    if (!wait_one(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL))
+                        return false;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss<false>(tS, kmaj(sK, kk), kmaj(sQ, kk), T::IDESC_SDP, kk > 0);
+                    if (t > 0) {  // dQ_{t-1} must have left the dP^T columns
+                        if (!wait_one(b_dq_empty, (t - 1) & 1, abort_flag, prm.st, SITE_DQ_EMPTY))
+                            return false;
+                        tc_fence_after();
+                    }
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_ss<false>(tDP, kmaj(sV, kk), kmaj(sDO, kk), T::IDESC_SDP, kk > 0);
+                    mma_commit(b_s_full);
+                    if (!wait_one(b_p_full, t & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                    tc_fence_after();
+                    // dQ_i = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss<false>(tDP, mnmaj(sDS, kk), mnmaj(sK, kk), T::IDESC_DQ, kk > 0);
+                    mma_commit(b_dq_full);
+                    // dV += P^T dO_i : A = P^T in tensor memory, B = dO_i (MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ts<false>(tDV, tS + kk * 8, mnmaj(sDO, kk), T::IDESC_DV, (t > 0 || kk > 0));
+                    // dK += dS^T Q_i : A = dS^T (K-major), B = Q_i (MN-major)
+#pragma unroll
+                    for (int kk = 0; kk < kTile / 16; ++kk)
+                        mma_ss<false>(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), T::IDESC_DK, (t > 0 || kk > 0));
+                    mma_commit(b_qdo_empty(s));
+                }
+                mma_commit(b_dkv_full);
+                return true;
+            };
+            run();
+            mma_commit(b_done);
+            wait_drain(b_done, 0, prm.st, SITE_DRAIN);
+        }
+    } else if (warp < 4) {
+        // ================= compute warpgroup: P^T, dS^T =================
+        const int r = warp * 32 + lane;  // key row within the tile
+        const int kv_row = j * kTile + r;
+        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t tS = tmem + T::COL_S + lane_off, tDP = tmem + T::COL_DP + lane_off;
+        const float cs = prm.cs;
+        uint8_t* ds_row = smem + T::OFF_DS + r * 128;
+        const int sw = r & 7;
+        bool ok = true;
+        for (int t = 0; t < n_steps; ++t) {
+            const int s = t % T::STAGES;
+            const int i = i0 + t;
+            const float* lse2 = reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024);
+            const float* dsum = lse2 + 128;
+            // LSE2_i and D_i arrived with Q_i/dO_i; waiting here (the phase is already
+            // complete) makes those bulk-copied bytes visible to this thread.
+            if (!wait_warp(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL) ||
+                !wait_warp(b_s_full, t & 1, abort_flag, prm.st, SITE_S_FULL)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // diagonal tile: query column c visible iff c >= r
+            const int cmin = (prm.causal && i == j) ? r : 0;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {  // two halves of 64 query columns
+                uint32_t pk[32];
+#pragma unroll
+                for (int cc = 0; cc < 2; ++cc) {
+                    const int c0 = h * 64 + cc * 32;
+                    uint32_t sv[32], dp[32];
+                    tmem_ld32(tS + c0, sv);
+                    tmem_ld32(tDP + c0, dp);
+                    tmem_ld_wait(sv);
+                    tmem_ld_wait(dp);
+                    uint32_t dsw[16];
+#pragma unroll
+                    for (int e = 0; e < 32; e += 2) {
+                        const int c = c0 + e;
+                        float p0 = ex2_approx(fmaf(u2f(sv[e]), cs, -lse2[c]));
+                        float p1 = ex2_approx(fmaf(u2f(sv[e + 1]), cs, -lse2[c + 1]));
+                        if (c < cmin) p0 = 0.f;
+                        if (c + 1 < cmin) p1 = 0.f;
+                        pk[cc * 16 + e / 2] = pack_bf16x2(p0, p1);
+                        const float d0 = p0 * (u2f(dp[e]) - dsum[c]);
+                        const float d1 = p1 * (u2f(dp[e + 1]) - dsum[c + 1]);
+                        dsw[e / 2] = pack_bf16x2(d0, d1);
+                    }
+                    // 64 bytes of dS^T row r -> 16-byte chunks x = (c0 % 64) / 8 .. +3, swizzled
+                    uint8_t* blk = ds_row + (c0 / 64) * T::BLK_BYTES;
+                    const int x0 = (c0 & 63) / 8;
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        *reinterpret_cast<uint4*>(blk + (((x0 + v) ^ sw) << 4)) =
+                            make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3]);
+                }
+                tmem_st32(tS + 32 * h, pk);
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p_full);
+        }
+        // ---- epilogue: dV, dK (scaled) -> bf16 ----
+        if (ok && wait_warp(b_dkv_full, 0, abort_flag, prm.st, SITE_DKV)) {
+            tc_fence_after();
+            const bool row_ok = kv_row < N;
+            const size_t roff = (static_cast<size_t>(bh) * N + (row_ok ? kv_row : 0)) * D * 2;
+#pragma unroll
+            for (int which = 0; which < 2; ++which) {
+                const uint32_t tsrc = tmem + (which ? T::COL_DK : T::COL_DV) + lane_off;
+                uint8_t* dst = static_cast<uint8_t*>(which ? prm.dk : prm.dv) + roff;
+                const float f = which ? prm.scale : 1.f;
+#pragma unroll
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tsrc + 32 * c, o);
+                    tmem_ld_wait(o);
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f);
+                    if (row_ok) {
+#pragma unroll
+                        for (int v = 0; v < 4; ++v)
+                            st_global_v4(dst + c * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                         pk[4 * v + 3]);
+                    }
+                }
+            }
+        }
+    } else {
+        // ================= dQ writer warpgroup =================
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // query row within tile i
+        const uint32_t tDQ = tmem + T::COL_DP + (static_cast<uint32_t>(wq * 32) << 16);
+        for (int t = 0; t < n_steps; ++t) {
+            const int i = i0 + t;
+            if (!wait_warp(b_dq_full, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) break;
+            tc_fence_after();
+            float* dst = prm.dq_acc + (static_cast<size_t>(bh) * prm.Npad + i * kTile + r) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld32(tDQ + 32 * c, v);
+                tmem_ld_wait(v);
+                if (c == D / 32 - 1) {  // the tile has left tensor memory
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_dq_empty);
+                }
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    red_add_v4(dst + c * 32 + e, u2f(v[e]), u2f(v[e + 1]), u2f(v[e + 2]), u2f(v[e + 3]));
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 9) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+    using T = BwdTraits<D>;
+    static const cudaError_t attr = cudaFuncSetAttribute(
+        bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+    if (attr != cudaSuccess) return attr;
+    const long long grid = static_cast<long long>(p.BH) * p.n_kv;
+    bwd_main_kernel<D><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.BH) * p.Npad;
+    const long long blocks = (rows + 7) / 8;
+    const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
+    bwd_pre_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
+    const long long total = static_cast<long long>(p.BH) * p.N * (p.D / 8);
+    const long long blocks = (total + 255) / 256;
+    const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
+    dq_convert_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+    if (D == 64) return launch_bwd_main_impl<64>(tq, tk, tv, tdo, p, stream);
+    if (D == 128) return launch_bwd_main_impl<128>(tq, tk, tv, tdo, p, stream);
+    return cudaErrorInvalidValue;
+}
+
+int bwd_smem_bytes(int D) {
+    if (D == 64) return BwdTraits<64>::SMEM_BYTES;
+    if (D == 128) return BwdTraits<128>::SMEM_BYTES;
+    return 0;
+}
+
+}  // namespace attn

@@ -1,0 +1,73 @@
+// Parameter blocks and launcher entry points shared by the host-side C ABI
+// (attn_api.cu) and the kernel translation units.  Internal: not installed.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn_device_status.cuh"
+
+namespace attn {
+
+constexpr int kTile = 128;  // rows of Q, K, V per tile (M and N of every MMA)
+
+struct FwdParams {
+    void* o;          // bf16 [BH, N, D]
+    float* lse;       // fp32 [BH, N], natural log of the row normaliser
+    int N;            // sequence length (queries = keys)
+    int BH;           // batch * heads
+    int n_pairs;      // ceil(N / 256): CTAs per head (two 128-row Q tiles each)
+    int causal;       // 1: key j visible to query i iff j <= i
+    float cs;         // scale * log2(e) (fp8: scale * s_q * s_k * log2(e))
+    float out_scale;  // 1 (bf16) or s_v (fp8)
+    DevStatus st;
+};
+
+struct BwdPreParams {
+    const void* o;     // bf16 [BH, N, D]
+    const void* dout;  // bf16 [BH, N, D]
+    const float* lse;  // fp32 [BH, N]
+    float* dq_acc;     // fp32 [BH, Npad, D], zeroed here
+    float* lse2;       // fp32 [BH, Npad]: LSE * log2(e); +inf on padding rows
+    float* dsum;       // fp32 [BH, Npad]: D_i = sum_k dO_ik O_ik; 0 on padding rows
+    int N, Npad, BH, D;
+};
+
+struct BwdParams {
+    const float* lse2;  // workspace, see BwdPreParams
+    const float* dsum;
+    float* dq_acc;
+    void* dk;           // bf16 [BH, N, D]
+    void* dv;           // bf16 [BH, N, D]
+    int N, Npad, BH;
+    int n_kv;           // ceil(N / 128): CTAs per head
+    int causal;
+    float cs;           // scale * log2(e)
+    float scale;        // softmax scale (applied to dK here and to dQ at conversion)
+    DevStatus st;
+};
+
+struct DqConvertParams {
+    const float* dq_acc;  // fp32 [BH, Npad, D]
+    void* dq;             // bf16 [BH, N, D]
+    int N, Npad, BH, D;
+    float scale;
+};
+
+// Launchers (return the launch's cudaError_t; no synchronisation).
+cudaError_t launch_fwd_bf16(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_fwd_fp8(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                           const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
+cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                            cudaStream_t stream);
+cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream);
+cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream);
+
+// Shared-memory bytes a launcher requests (for tests of the host logic).
+int fwd_smem_bytes(int D, bool fp8);
+int bwd_smem_bytes(int D);
+
+}  // namespace attn

@@ -1,0 +1,146 @@
+/*
+ * attn_sm103a.h -- C ABI of libattn_sm103a.so: exact softmax attention on one
+ * NVIDIA GB300 (sm_103a), forward, backward and FP8 forward.
+ *
+ * What is computed (per batch b and head h, all rows independent):
+ *   S = scale * Q K^T, with the causal mask "key j visible to query i iff
+ *   j <= i" when causal = 1; P = softmax(S) row-wise; O = P V;
+ *   LSE_i = ln(sum_j exp(S_ij)) (natural log, of the scaled scores).
+ * The forward pass is tiled with the online-softmax recurrence -- running
+ * maximum and running sum of exponentials, combined after rescaling to a
+ * common maximum, with the same rescale applied to the output accumulator --
+ * so the N x N matrices S and P are never written to memory
+ * (xtrax digest "q02 FlashAttention", sections 1-2; ai.engineer topic page,
+ * items 57 "Online Normalizer Calculation for Softmax" and 58
+ * "FlashAttention").  The backward pass recomputes P from Q, K and the saved
+ * LSE (item 58) and uses dV = P^T dO, dP = dO V^T, D_i = sum_k dO_ik O_ik,
+ * dS = P * (dP - D), dQ = scale dS K, dK = scale dS^T Q.
+ *
+ * Conventions shared by every entry point:
+ *  - Layout: Q, K, V, O, dO, dQ, dK, dV are dense row-major [B, H, N, d]
+ *    (d contiguous); LSE is dense [B, H, N].  Sequence lengths of queries and
+ *    keys are equal (N).  d is 64 or 128 (FP8: 128).
+ *  - Pointers are DEVICE pointers, 16-byte aligned, owned by the caller; the
+ *    library allocates nothing and keeps no pointer after a call returns.
+ *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream);
+ *    nothing synchronises.  Outputs are valid once the stream reaches that
+ *    point.
+ *  - Errors are returned, never thrown or printed.  Invalid arguments return
+ *    ATTN_ERR_INVALID (or ATTN_ERR_UNSUPPORTED for a valid but unbuilt shape
+ *    or a device other than sm_103) before anything is launched.  A launch
+ *    failure returns ATTN_ERR_CUDA.  Kernels never trap: a pipeline wait that
+ *    does not complete within the wait limit (default 1 s) makes the kernel
+ *    record the fact and return; attn_check_device_error() reports it.
+ */
+#ifndef ATTN_SM103A_H_
+#define ATTN_SM103A_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID = -1,     /* bad pointer, size, alignment or scale */
+    ATTN_ERR_UNSUPPORTED = -2, /* d or dtype not built, or device is not sm_103 */
+    ATTN_ERR_CUDA = -3,        /* a CUDA runtime or driver call failed */
+    ATTN_ERR_TIMEOUT = -4      /* a kernel's bounded wait gave up (device error word) */
+} attn_status;
+
+/*
+ * Forward pass, bf16 in and out, fp32 accumulation.
+ *   q, k, v : bf16 [B, H, N, d] inputs.
+ *   o       : bf16 [B, H, N, d] output, O = P V rounded to nearest even.
+ *   lse     : fp32 [B, H, N] output, natural log-sum-exp of the scaled scores
+ *             (the statistic attn_bwd consumes).
+ *   scale   : softmax scale, finite and > 0 (usually 1/sqrt(d)).
+ *   causal  : 0 or 1.
+ * Source: FlashAttention digest sections 1-2 (tiling, online softmax, fused
+ * single kernel); ai.engineer items 41 (query-row tiles across blocks, delayed
+ * normalisation), 58, 59 (causal mask) and 60 (-inf guards).
+ */
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int H, int N, int d, float scale, int causal, attn_stream_t stream);
+
+/*
+ * Bytes of device scratch attn_bwd needs for (B, H, N, d): an fp32 dQ
+ * accumulator [B*H, Npad, d] plus two fp32 vectors [B*H, Npad] (LSE in log2
+ * units and D), Npad = N rounded up to 128.  Returns 0 for invalid sizes.
+ */
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
+
+/*
+ * Backward pass for O = softmax(scale Q K^T [+mask]) V.
+ *   q, k, v, o, dout : bf16 [B, H, N, d] inputs (o and lse from attn_fwd).
+ *   lse              : fp32 [B, H, N] from attn_fwd.
+ *   dq, dk, dv       : bf16 [B, H, N, d] outputs.
+ *   workspace        : device scratch of attn_bwd_workspace_bytes() bytes,
+ *                      256-byte aligned, caller-owned; overwritten.
+ * Three kernels run in order on `stream`: preprocess (D, LSE, zeroed dQ
+ * accumulator), main (recompute P, accumulate dV, dK in tensor memory, add
+ * dQ partial tiles into the accumulator with fp32 reductions), and dQ
+ * conversion.  dQ's summation order varies from run to run (scatter-add
+ * item 52); dK and dV are deterministic.
+ * Source: ai.engineer item 58 (backward regenerates score tiles from saved
+ * normalisation statistics); FlashAttention-3 digest section 1 (dQ-writer
+ * warp and atomic accumulation); the gradient formulas are the calculus of
+ * the forward definition (the pages' own statement of them is cut off).
+ */
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace, int B,
+                     int H, int N, int d, float scale, int causal, attn_stream_t stream);
+
+/*
+ * FP8 forward pass: OCP E4M3 inputs with per-tensor fp32 scales.
+ *   q8, k8, v8 : uint8 E4M3 codes [B, H, N, d]; the value read is s * code
+ *                (sq, sk, sv finite and > 0).
+ *   o          : bf16 [B, H, N, d] output; lse : fp32 [B, H, N] as attn_fwd.
+ * Scores use fp32 accumulation of the E4M3 products; P is rounded to E4M3
+ * (saturating) before the P V product, which accumulates in fp32.  d = 128.
+ * Source: FlashAttention-3 digest (FP8 forward); ai.engineer item 33
+ * (affine quantisation r = S(q - Z), here Z = 0).
+ */
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float sq, float sk,
+                         float sv, void* o, float* lse, int B, int H, int N, int d, float scale,
+                         int causal, attn_stream_t stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the library's device error
+ * word on the current device.  Returns ATTN_ERR_TIMEOUT if any kernel's
+ * bounded wait gave up since the last check (the results of that launch are
+ * undefined), ATTN_ERR_CUDA if synchronisation failed, else ATTN_OK.
+ * `site` (may be NULL) receives the id of the first wait that gave up.
+ */
+attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site);
+
+/*
+ * Wait limit, in nanoseconds, that every pipeline wait of later launches
+ * uses before it gives up (default 1e9).  0 restores the default.
+ */
+void attn_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Self-test of the bounded-wait path: launches one CTA whose warps wait on a
+ * barrier nothing ever completes, with the current wait limit.  The kernel
+ * returns after the limit; attn_check_device_error() must then report
+ * ATTN_ERR_TIMEOUT.  No fault, trap or hang is involved.
+ */
+attn_status attn_selftest_wait_timeout(attn_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char* attn_status_string(attn_status s);
+
+/* Dynamic shared memory (bytes) one CTA of the given kernel requests:
+ * which = 0 forward bf16, 1 forward fp8, 2 backward main; 0 if not built. */
+int attn_kernel_smem_bytes(int which, int d);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_SM103A_H_ */
