@@ -1,0 +1,430 @@
+#!/usr/bin/env python
+"""Benchmark of the exact-attention hot path on GB300.
+
+One step = the whole path once:
+  * bf16 forward + backward (preprocess, main, dQ conversion) on
+    B=1, H=32, N=8192, d=128, non-causal, 1% of key rows scaled x8;
+  * FP8 (E4M3, per-tensor scales) forward on B=1, H=16, N=16384, d=128, causal.
+Metric: attention TFLOP/s (forward 4*B*H*N^2*d, halved when causal; backward
+2.5x the forward), whole job over all ranks.  Inputs are seeded synthetic
+N(0,1) draws (no dataset involved); together they exceed the 129 MB L2, so
+no flush is done between steps.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on a bounded sample of the same workload on the host cores.
+For N > 1 (torchrun), every rank runs its own copy of the workload (weak
+scaling over independent (batch, head) problems; no collective on the data
+path) and rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from exact_attention_52_gb300.roofline import attn_bytes, attn_flops  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s on 1xGB300 (bf16, fp8 fwd) and % of dense tensor peak"
+BF16 = dict(B=1, H=32, N=8192, d=128, causal=False, outlier_frac=0.01, outlier_factor=8.0)
+FP8 = dict(B=1, H=16, N=16384, d=128, causal=True)
+WORKLOAD = ("fwd+bwd bf16 B1 H32 N8192 d128 (1% keys x8) + fp8 fwd B1 H16 N16384 d128 causal")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+
+
+def step_flops():
+    fb = attn_flops(BF16["B"], BF16["H"], BF16["N"], BF16["d"], BF16["causal"])
+    f8 = attn_flops(FP8["B"], FP8["H"], FP8["N"], FP8["d"], FP8["causal"])
+    return {"fwd": fb, "bwd": 2.5 * fb, "fwd_fp8": f8}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_sources_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "exact_attention_52_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, or None when the
+    kernel sources changed after the capture."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            t = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = t.get(kernel_key)
+    if not e or e.get("sources_sha") != kernel_sources_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 7:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[3:7]):
+                    if v.lower() == "active":
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# CPU side: the oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+
+
+def oracle_sample_step(data):
+    """One bounded sample of the workload through the fp64 oracle: one head of
+    the bf16 forward + backward and 256 query rows of one FP8 head.  Returns
+    the attention FLOPs it covers (same convention as the GPU)."""
+    import oracle
+    q, k, v, do = data["bf16"]
+    s = 1.0 / math.sqrt(BF16["d"])
+    oracle.forward(q, k, v, s, BF16["causal"], heads=[(0, 0)])
+    oracle.backward(q, k, v, do, s, BF16["causal"], heads=[(0, 0)])
+    q8, k8, v8 = data["fp8"]
+    rows = data["fp8_rows"]
+    oracle.forward(q8, k8, v8, s, FP8["causal"], heads=[(0, 0)], rows=rows)
+    N = BF16["N"]
+    f = 4.0 * N * N * BF16["d"] * 3.5
+    # causal rows i see i+1 keys: 2*(i+1)*d multiply-adds for each of S and PV
+    f += sum(4.0 * (int(i) + 1) * FP8["d"] for i in rows)
+    return f
+
+
+def oracle_sample_data():
+    import numpy as np
+
+    import oracle
+    from exact_attention_52_gb300.inputs import make_inputs, make_inputs_fp8
+    inp = make_inputs(1, 1, BF16["N"], BF16["d"], seed=0, with_grad=True,
+                      outlier_frac=BF16["outlier_frac"], outlier_factor=BF16["outlier_factor"])
+    bf = tuple(oracle.bf16_bits_to_f64(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    f8 = make_inputs_fp8(1, 1, FP8["N"], FP8["d"], seed=0)
+    f8v = (oracle.e4m3_to_f64(f8.q8, f8.sq), oracle.e4m3_to_f64(f8.k8, f8.sk),
+           oracle.e4m3_to_f64(f8.v8, f8.sv))
+    rows = np.linspace(0, FP8["N"] - 1, 256).astype(np.int64)
+    return {"bf16": bf, "fp8": f8v, "fp8_rows": rows}
+
+
+SAMPLE_DESC = ("fp64 oracle, explicit S and P: head 0 of the bf16 workload (forward + backward, "
+               "N=8192) and 256 evenly spaced query rows of head 0 of the FP8 workload")
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    data = oracle_sample_data()
+    for _ in range(args.warmup):
+        oracle_sample_step(data)
+    t0 = time.perf_counter()
+    flops = 0.0
+    for _ in range(args.steps):
+        flops += oracle_sample_step(data)
+    dt = time.perf_counter() - t0
+    value = flops / dt / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
+                         "kind": "oracle", "sample": SAMPLE_DESC},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU side
+# ---------------------------------------------------------------------------
+
+
+def make_device_data(torch, dev):
+    import numpy as np
+
+    from exact_attention_52_gb300.inputs import make_inputs, make_inputs_fp8
+    inp = make_inputs(BF16["B"], BF16["H"], BF16["N"], BF16["d"], seed=0, with_grad=True,
+                      outlier_frac=BF16["outlier_frac"], outlier_factor=BF16["outlier_factor"])
+
+    def host_bf16(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+
+    h = {n: host_bf16(getattr(inp, n + "_bits")).pin_memory() for n in ("q", "k", "v", "do")}
+    f8 = make_inputs_fp8(FP8["B"], FP8["H"], FP8["N"], FP8["d"], seed=0)
+    for n in ("q8", "k8", "v8"):
+        h[n] = torch.from_numpy(getattr(f8, n)).pin_memory()
+    d = {n: t.to(dev) for n, t in h.items()}
+    d["scales"] = (f8.sq, f8.sk, f8.sv)
+    return h, d
+
+
+def run_ours(args):
+    import torch
+
+    from exact_attention_52_gb300 import api
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        data = oracle_sample_data()
+        t0 = time.perf_counter()
+        f = oracle_sample_step(data)
+        dt = time.perf_counter() - t0
+        cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
+               "sample": SAMPLE_DESC + f" (one pass, {dt:.1f} s)"}
+        del data
+
+    host, d = make_device_data(torch, dev)
+    B, H, N, D = BF16["B"], BF16["H"], BF16["N"], BF16["d"]
+    scale = 1.0 / math.sqrt(D)
+    o = torch.empty_like(d["q"])
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(o), torch.empty_like(o), torch.empty_like(o)
+    ws = torch.empty(api.bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device=dev)
+    B8, H8, N8 = FP8["B"], FP8["H"], FP8["N"]
+    o8 = torch.empty((B8, H8, N8, FP8["d"]), dtype=torch.bfloat16, device=dev)
+    lse8 = torch.empty((B8, H8, N8), dtype=torch.float32, device=dev)
+    sq, sk, sv = d["scales"]
+    stream = torch.cuda.current_stream()
+    KERNELS = ("fwd", "bwd_pre", "bwd_main", "bwd_dq_convert", "fwd_fp8")
+
+    def step(ev=None):
+        e = ev or [None] * 8
+        if e[0] is not None:
+            e[0].record(stream)
+        api.fwd(d["q"], d["k"], d["v"], scale=scale, causal=BF16["causal"], o=o, lse=lse)
+        api.bwd_stages(d["q"], d["k"], d["v"], o, d["do"], lse, dq, dk, dv, ws, scale,
+                       BF16["causal"], events=e[1:5])
+        api.fwd_fp8(d["q8"], d["k8"], d["v8"], sq, sk, sv, scale=scale, causal=FP8["causal"],
+                    o=o8, lse=lse8)
+        if e[5] is not None:
+            e[5].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    rc, site = api.check_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} at wait site {site:#x}")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(torch.cuda.current_device())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    rc, site = api.check_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} at wait site {site:#x}")
+    elapsed_ms = t_start.elapsed_time(t_end)
+
+    # per-kernel averages from the events inside the timed region
+    def avg(a, b):
+        return sum(evs[i][a].elapsed_time(evs[i][b]) for i in range(args.steps)) / args.steps
+    k_ms = {"fwd": avg(0, 1), "bwd_pre": avg(1, 2), "bwd_main": avg(2, 3),
+            "bwd_dq_convert": avg(3, 4), "fwd_fp8": avg(4, 5)}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not args.no_e2e:
+        outs = [o, lse, dq, dk, dv, o8, lse8]
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
+        ins = ("q", "k", "v", "do", "q8", "k8", "v8")
+        h2d = sum(host[n].numel() * host[n].element_size() for n in ins)
+        d2h = sum(t.numel() * t.element_size() for t in outs)
+        n_e2e = max(1, min(args.steps, 10))
+        torch.cuda.synchronize()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(n_e2e):
+            for n in ins:
+                d[n].copy_(host[n], non_blocking=True)
+            step()
+            for hb, t in zip(host_out, outs):
+                hb.copy_(t, non_blocking=True)
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = a.elapsed_time(b) / n_e2e
+        e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+
+    times = torch.tensor([elapsed_ms, e2e["ms_per_step"] if e2e else 0.0], device=dev)
+    if dist:
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    elapsed_ms = float(times[0])
+    flops = step_flops()
+    total_flops = sum(flops.values()) * world
+    ms_per_step = elapsed_ms / args.steps
+    value = total_flops / (ms_per_step * 1e-3) / 1e12
+
+    if rank != 0:
+        if dist:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_kind = load_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    bwd_main_flops = flops["bwd"]
+    achieved = bwd_main_flops / (k_ms["bwd_main"] * 1e-3) / 1e12
+    traffic = recorded_traffic("bwd_main_b1_h32_n8192_d128")
+    components = {}
+    for name, f, kms in (("fwd", flops["fwd"], k_ms["fwd"]),
+                         ("bwd", flops["bwd"], k_ms["bwd_pre"] + k_ms["bwd_main"] + k_ms["bwd_dq_convert"]),
+                         ("fwd_fp8", flops["fwd_fp8"], k_ms["fwd_fp8"])):
+        tf = f / (kms * 1e-3) / 1e12
+        pk = (2.0 if name == "fwd_fp8" else 1.0)
+        components[name] = {"ms": round(kms, 4), "tflops": round(tf, 1),
+                            "frac_of_sustained": round(tf / (pk * sustained), 4),
+                            "frac_of_burst": round(tf / (pk * burst), 4)}
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16+e4m3",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "l2": "inputs 0.54 GB > 129 MB L2, no flush",
+                   "parallelism": f"replicas x{world} (independent heads, no collective)"},
+        "components": components,
+        "kernel_ms": {k: round(v, 4) for k, v in k_ms.items()},
+        "roofline": {"kernel": "bwd_main (attn_bwd_main)", "bound": "tensor",
+                     "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
+                     "frac": round(achieved / sustained, 4),
+                     "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
+                     "traffic": traffic,
+                     "algorithmic_bytes": attn_bytes(B, H, N, D, "bwd")},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clk,
+        "cpu_baseline": cpu,
+        "e2e": None if e2e is None else {
+            "value": round(total_flops / (e2e["ms_per_step"] * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+            "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+            "ms_per_step": round(e2e["ms_per_step"], 4)},
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the oracle timing (used for profiling runs)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -26,6 +26,9 @@ SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
     "attn_bwd": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "attn_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
+    "attn_bwd_main": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
+    "attn_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_check_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
@@ -172,3 +175,31 @@ def set_wait_limit_ns(ns: int) -> None:
 def selftest_wait_timeout(stream=None) -> None:
     _check("attn_selftest_wait_timeout",
            load_library().attn_selftest_wait_timeout(_stream_handle(stream)))
+
+
+def bwd_stages(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causal: bool,
+               stream=None, events=None):
+    """attn_bwd as its three C-ABI stages; ``events`` (4 CUDA events, optional)
+    are recorded before, between and after them on the same stream."""
+    B, H, N, d = q.shape
+    lib = load_library()
+    h = _stream_handle(stream)
+    c = int(bool(causal))
+    ev = events or [None] * 4
+    if ev[0] is not None:
+        ev[0].record(stream)
+    _check("attn_bwd_preprocess", lib.attn_bwd_preprocess(o.data_ptr(), dout.data_ptr(),
+                                                          lse.data_ptr(), workspace.data_ptr(),
+                                                          B, H, N, d, h))
+    if ev[1] is not None:
+        ev[1].record(stream)
+    _check("attn_bwd_main", lib.attn_bwd_main(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                              dout.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                              workspace.data_ptr(), B, H, N, d, float(scale), c, h))
+    if ev[2] is not None:
+        ev[2].record(stream)
+    _check("attn_bwd_dq_convert", lib.attn_bwd_dq_convert(dq.data_ptr(), workspace.data_ptr(),
+                                                          B, H, N, d, float(scale), h))
+    if ev[3] is not None:
+        ev[3].record(stream)
+    return dq, dk, dv

@@ -233,9 +233,114 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
     return bwd_layout(B, H, N, d).total;
 }
 
+namespace {
+
+// Validated view of the backward workspace.
+struct BwdCall {
+    DeviceState* ds = nullptr;
+    float* dq_acc = nullptr;
+    float* lse2 = nullptr;
+    float* dsum = nullptr;
+    int BH = 0, Np = 0;
+};
+
+attn_status bwd_prepare(void* workspace, int B, int H, int N, int d, float scale, int causal,
+                        BwdCall* c) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_INVALID;
+    if ((rc = device_state(&c->ds)) != ATTN_OK) return rc;
+    const BwdLayout L = bwd_layout(B, H, N, d);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    c->dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
+    c->lse2 = reinterpret_cast<float*>(ws + L.lse2);
+    c->dsum = reinterpret_cast<float*>(ws + L.dsum);
+    c->BH = B * H;
+    c->Np = static_cast<int>(npad(N));
+    return ATTN_OK;
+}
+
+}  // namespace
+
+attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
+                                int B, int H, int N, int d, attn_stream_t stream) {
+    for (const void* p : {o, dout, static_cast<const void*>(lse)})
+        if (!aligned16(p)) return ATTN_ERR_INVALID;
+    BwdCall c;
+    attn_status rc = bwd_prepare(workspace, B, H, N, d, 1.f, 0, &c);
+    if (rc != ATTN_OK) return rc;
+    BwdPreParams pp;
+    pp.o = o;
+    pp.dout = dout;
+    pp.lse = lse;
+    pp.dq_acc = c.dq_acc;
+    pp.lse2 = c.lse2;
+    pp.dsum = c.dsum;
+    pp.N = N;
+    pp.Npad = c.Np;
+    pp.BH = c.BH;
+    pp.D = d;
+    return launch_bwd_pre(pp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
+                                                                                     : ATTN_ERR_CUDA;
+}
+
+attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                          void* dv, void* workspace, int B, int H, int N, int d, float scale,
+                          int causal, attn_stream_t stream) {
+    for (const void* p : {q, k, v, dout, static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (!aligned16(p)) return ATTN_ERR_INVALID;
+    BwdCall c;
+    attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, causal, &c);
+    if (rc != ATTN_OK) return rc;
+    CUtensorMap tq, tk, tv, tdo;
+    if (!make_map(&tq, q, false, d, N, c.BH) || !make_map(&tk, k, false, d, N, c.BH) ||
+        !make_map(&tv, v, false, d, N, c.BH) || !make_map(&tdo, dout, false, d, N, c.BH))
+        return ATTN_ERR_CUDA;
+    BwdParams bp;
+    bp.lse2 = c.lse2;
+    bp.dsum = c.dsum;
+    bp.dq_acc = c.dq_acc;
+    bp.dk = dk;
+    bp.dv = dv;
+    bp.N = N;
+    bp.Npad = c.Np;
+    bp.BH = c.BH;
+    bp.n_kv = (N + kTile - 1) / kTile;
+    bp.causal = causal;
+    bp.cs = scale * 1.44269504088896340736f;
+    bp.scale = scale;
+    bp.st = dev_status(c.ds);
+    return launch_bwd_main(d, tq, tk, tv, tdo, bp, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, int d, float scale,
+                                attn_stream_t stream) {
+    if (!aligned16(dq)) return ATTN_ERR_INVALID;
+    BwdCall c;
+    attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, 0, &c);
+    if (rc != ATTN_OK) return rc;
+    DqConvertParams cp;
+    cp.dq_acc = c.dq_acc;
+    cp.dq = dq;
+    cp.N = N;
+    cp.Npad = c.Np;
+    cp.BH = c.BH;
+    cp.D = d;
+    cp.scale = scale;
+    return launch_dq_convert(cp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
 attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
                      const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
                      int N, int d, float scale, int causal, attn_stream_t stream) {
+    // Validate everything before the first launch so that a bad argument
+    // leaves the stream untouched.
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
     for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
@@ -243,61 +348,11 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
         if (!aligned16(p)) return ATTN_ERR_INVALID;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return ATTN_ERR_INVALID;
-    DeviceState* ds = nullptr;
-    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-    const int BH = B * H;
-    const BwdLayout L = bwd_layout(B, H, N, d);
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    float* dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
-    float* lse2 = reinterpret_cast<float*>(ws + L.lse2);
-    float* dsum = reinterpret_cast<float*>(ws + L.dsum);
-    const int Np = static_cast<int>(npad(N));
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-    CUtensorMap tq, tk, tv, tdo;
-    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, BH) ||
-        !make_map(&tv, v, false, d, N, BH) || !make_map(&tdo, dout, false, d, N, BH))
-        return ATTN_ERR_CUDA;
-
-    BwdPreParams pp;
-    pp.o = o;
-    pp.dout = dout;
-    pp.lse = lse;
-    pp.dq_acc = dq_acc;
-    pp.lse2 = lse2;
-    pp.dsum = dsum;
-    pp.N = N;
-    pp.Npad = Np;
-    pp.BH = BH;
-    pp.D = d;
-    if (launch_bwd_pre(pp, st) != cudaSuccess) return ATTN_ERR_CUDA;
-
-    BwdParams bp;
-    bp.lse2 = lse2;
-    bp.dsum = dsum;
-    bp.dq_acc = dq_acc;
-    bp.dk = dk;
-    bp.dv = dv;
-    bp.N = N;
-    bp.Npad = Np;
-    bp.BH = BH;
-    bp.n_kv = (N + kTile - 1) / kTile;
-    bp.causal = causal;
-    bp.cs = scale * 1.44269504088896340736f;
-    bp.scale = scale;
-    bp.st = dev_status(ds);
-    if (launch_bwd_main(d, tq, tk, tv, tdo, bp, st) != cudaSuccess) return ATTN_ERR_CUDA;
-
-    DqConvertParams cp;
-    cp.dq_acc = dq_acc;
-    cp.dq = dq;
-    cp.N = N;
-    cp.Npad = Np;
-    cp.BH = BH;
-    cp.D = d;
-    cp.scale = scale;
-    if (launch_dq_convert(cp, st) != cudaSuccess) return ATTN_ERR_CUDA;
-    return ATTN_OK;
+    if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
+    if ((rc = attn_bwd_main(q, k, v, dout, dk, dv, workspace, B, H, N, d, scale, causal, stream)) !=
+        ATTN_OK)
+        return rc;
+    return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
 }
 
 attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site) {

@@ -96,6 +96,26 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
                      int H, int N, int d, float scale, int causal, attn_stream_t stream);
 
 /*
+ * The three stages of attn_bwd, for callers that schedule or time them
+ * separately.  They must run in this order on one stream with the same
+ * workspace and sizes; attn_bwd is exactly these three calls.
+ *   attn_bwd_preprocess : D_i = sum_k dO_ik O_ik, LSE in log2 units, padded
+ *                         rows, and a zeroed fp32 dQ accumulator, all in the
+ *                         workspace.  Reads o, dout, lse.
+ *   attn_bwd_main       : recomputes P, writes dk, dv (bf16) and adds every
+ *                         partial dQ tile into the workspace accumulator.
+ *   attn_bwd_dq_convert : dq = bf16(scale * accumulator).
+ * Same argument rules and errors as attn_bwd.
+ */
+attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
+                                int B, int H, int N, int d, attn_stream_t stream);
+attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                          void* dv, void* workspace, int B, int H, int N, int d, float scale,
+                          int causal, attn_stream_t stream);
+attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, int d, float scale,
+                                attn_stream_t stream);
+
+/*
  * FP8 forward pass: OCP E4M3 inputs with per-tensor fp32 scales.
  *   q8, k8, v8 : uint8 E4M3 codes [B, H, N, d]; the value read is s * code
  *                (sq, sk, sv finite and > 0).
