@@ -170,11 +170,20 @@ __global__ void __launch_bounds__(320, 1)
     }
 
     const int N = prm.N;
-    const int bh = blockIdx.x % prm.BH;
-    const int j = static_cast<int>(blockIdx.x / prm.BH);  // key tile; low j first (longest causal loops)
+    // Head-major order keeps the resident CTAs on a few heads, so those heads'
+    // Q, dO and fp32 dQ accumulator stay in L2 while every key tile reduces
+    // into them.  Within a head, low key tiles (longest causal loops) first.
+    const int bh = static_cast<int>(blockIdx.x / prm.n_kv);
+    const int j = static_cast<int>(blockIdx.x % prm.n_kv);  // key tile
     const int n_q_total = (N + kTile - 1) / kTile;
-    const int i0 = prm.causal ? j : 0;
-    const int n_steps = n_q_total - i0;
+    const int n_steps = prm.causal ? n_q_total - j : n_q_total;
+    // Query tile of step t.  Causal: the diagonal tile j, then upwards.
+    // Otherwise each key tile starts at its own index and wraps, so CTAs that
+    // run together reduce into different dQ tiles.
+    auto q_tile = [&](int t) {
+        const int i = j + t;
+        return (prm.causal || i < n_q_total) ? i : i - n_q_total;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
@@ -219,7 +228,7 @@ __global__ void __launch_bounds__(320, 1)
             int t = 0;
             for (; t < n_steps; ++t) {
                 const int s = t % T::STAGES;
-                const int i = i0 + t;
+                const int i = q_tile(t);
                 if (t >= T::STAGES &&
                     !wait_one(b_qdo_empty(s), ((t / T::STAGES) - 1) & 1, abort_flag, prm.st,
                               SITE_QDO_EMPTY))
@@ -311,7 +320,7 @@ __global__ void __launch_bounds__(320, 1)
         bool ok = true;
         for (int t = 0; t < n_steps; ++t) {
             const int s = t % T::STAGES;
-            const int i = i0 + t;
+            const int i = q_tile(t);
             const float* lse2 = reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024);
             const float* dsum = lse2 + 128;
             // LSE2_i and D_i arrived with Q_i/dO_i; waiting here (the phase is already
@@ -397,7 +406,7 @@ __global__ void __launch_bounds__(320, 1)
         const int r = wq * 32 + lane;  // query row within tile i
         const uint32_t tDQ = tmem + T::COL_DP + (static_cast<uint32_t>(wq * 32) << 16);
         for (int t = 0; t < n_steps; ++t) {
-            const int i = i0 + t;
+            const int i = q_tile(t);
             if (!wait_warp(b_dq_full, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) break;
             tc_fence_after();
             float* dst = prm.dq_acc + (static_cast<size_t>(bh) * prm.Npad + i * kTile + r) * D;

@@ -103,9 +103,12 @@ __global__ void __launch_bounds__(320, 1)
         return;
     }
 
-    // ---- work assignment: heaviest causal tiles are launched first ----
-    const int bh = blockIdx.x % prm.BH;
-    const int pair = prm.n_pairs - 1 - static_cast<int>(blockIdx.x / prm.BH);
+    // ---- work assignment ----
+    // Head-major order: the CTAs resident at any time cover only a few heads,
+    // so each head's K and V are read from HBM about once and then hit L2.
+    // Within a head the heaviest causal tiles come first.
+    const int bh = static_cast<int>(blockIdx.x / prm.n_pairs);
+    const int pair = prm.n_pairs - 1 - static_cast<int>(blockIdx.x % prm.n_pairs);
     const int N = prm.N;
     const int n_kv_total = (N + kTile - 1) / kTile;
     int n_t[2];
@@ -353,8 +356,11 @@ __global__ void __launch_bounds__(320, 1)
                         for (int i = 0; i < 32; i += 2) {
                             const float p0 = ex2_approx(fmaf(u2f(s[c][i]), cs, -m_sub));
                             const float p1 = ex2_approx(fmaf(u2f(s[c][i + 1]), cs, -m_sub));
-                            ls[(i >> 1) & 3] += p0 + p1;
-                            pk[cc * 16 + i / 2] = pack_bf16x2(p0, p1);
+                            const uint32_t w = pack_bf16x2(p0, p1);
+                            // The normaliser sums the same bf16 values that multiply V, so
+                            // O stays an exact convex combination of V rows.
+                            ls[(i >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+                            pk[cc * 16 + i / 2] = w;
                         }
                     }
                     tmem_st32(tS + 32 * h, pk);
