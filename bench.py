@@ -44,6 +44,7 @@ FP8 = dict(B=1, H=16, N=16384, d=128, causal=True)
 WORKLOAD = ("fwd+bwd bf16 B1 H32 N8192 d128 (1% keys x8) + fp8 fwd B1 H16 N16384 d128 causal")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+REF_BUDGET_S = 90.0  # wall time of the whole --impl reference run
 
 
 def step_flops():
@@ -145,22 +146,28 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 
 
-def oracle_sample_step(data):
-    """One bounded sample of the workload through the fp64 oracle: one head of
-    the bf16 forward + backward and 256 query rows of one FP8 head.  Returns
-    the attention FLOPs it covers (same convention as the GPU)."""
+def oracle_sample_step(data, n_rows):
+    """One bounded sample of the workload through the fp64 oracle: the forward
+    and backward work of ``n_rows`` evenly spaced query rows of head 0 of the
+    bf16 workload (non-causal, so a row subset is an exact slice of the work:
+    its S, P, dP, dS and dQ rows and its rank-``n_rows`` share of dK and dV),
+    plus 256 evenly spaced query rows of head 0 of the FP8 workload.  Returns
+    the attention FLOPs covered (same convention as the GPU)."""
+    import numpy as np
+
     import oracle
     q, k, v, do = data["bf16"]
-    s = 1.0 / math.sqrt(BF16["d"])
-    oracle.forward(q, k, v, s, BF16["causal"], heads=[(0, 0)])
-    oracle.backward(q, k, v, do, s, BF16["causal"], heads=[(0, 0)])
+    N, D = BF16["N"], BF16["d"]
+    rows = np.linspace(0, N - 1, n_rows).astype(np.int64)
+    s = 1.0 / math.sqrt(D)
+    oracle.head_forward(q[0, 0], k[0, 0], v[0, 0], s, False, rows=rows)
+    oracle.head_backward(q[0, 0][rows], k[0, 0], v[0, 0], do[0, 0][rows], s, False)
     q8, k8, v8 = data["fp8"]
-    rows = data["fp8_rows"]
-    oracle.forward(q8, k8, v8, s, FP8["causal"], heads=[(0, 0)], rows=rows)
-    N = BF16["N"]
-    f = 4.0 * N * N * BF16["d"] * 3.5
+    rows8 = data["fp8_rows"]
+    oracle.forward(q8, k8, v8, s, FP8["causal"], heads=[(0, 0)], rows=rows8)
+    f = 4.0 * n_rows * N * D * 3.5
     # causal rows i see i+1 keys: 2*(i+1)*d multiply-adds for each of S and PV
-    f += sum(4.0 * (int(i) + 1) * FP8["d"] for i in rows)
+    f += sum(4.0 * (int(i) + 1) * FP8["d"] for i in rows8)
     return f
 
 
@@ -179,8 +186,10 @@ def oracle_sample_data():
     return {"bf16": bf, "fp8": f8v, "fp8_rows": rows}
 
 
-SAMPLE_DESC = ("fp64 oracle, explicit S and P: head 0 of the bf16 workload (forward + backward, "
-               "N=8192) and 256 evenly spaced query rows of head 0 of the FP8 workload")
+def sample_desc(n_rows):
+    return (f"fp64 oracle, explicit S and P rows: forward + backward work of {n_rows} evenly spaced "
+            f"query rows of head 0 of the bf16 workload (N=8192, all keys) and 256 evenly spaced "
+            f"query rows of head 0 of the FP8 workload")
 
 
 def cpu_cores():
@@ -195,22 +204,28 @@ def run_reference(args):
     if rank != 0:
         return 0
     data = oracle_sample_data()
+    # Size each step so that warm-up + timed steps take about REF_BUDGET_S.
+    t0 = time.perf_counter()
+    oracle_sample_step(data, 256)
+    per_row = max((time.perf_counter() - t0) / 256, 1e-7)
+    n_rows = int(min(BF16["N"], max(64, REF_BUDGET_S / (args.steps + args.warmup) / per_row)))
     for _ in range(args.warmup):
-        oracle_sample_step(data)
+        oracle_sample_step(data, n_rows)
     t0 = time.perf_counter()
     flops = 0.0
     for _ in range(args.steps):
-        flops += oracle_sample_step(data)
+        flops += oracle_sample_step(data, n_rows)
     dt = time.perf_counter() - t0
     value = flops / dt / 1e12
+    desc = sample_desc(n_rows)
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "sample": SAMPLE_DESC},
+        "config": {"workload": WORKLOAD, "sample": desc},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cpu_cores(),
-                         "kind": "oracle", "sample": SAMPLE_DESC},
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -221,6 +236,21 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # GPU side
 # ---------------------------------------------------------------------------
+
+
+def max_over_ranks(values, dist=None, device=None):
+    """Element-wise maximum of per-rank timings (every rank gets the result)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    if dist is not None and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
+def whole_job_tflops(flops_per_rank, world, ms_per_step):
+    """Weak scaling: every rank processes its own copy of the step's work; the
+    job's throughput is the work of all ranks over the slowest rank's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
 
 
 def make_device_data(torch, dev):
@@ -262,11 +292,12 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         data = oracle_sample_data()
+        n_rows = BF16["N"]  # the whole of head 0: about 10-30 s of host work
         t0 = time.perf_counter()
-        f = oracle_sample_step(data)
+        f = oracle_sample_step(data, n_rows)
         dt = time.perf_counter() - t0
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": SAMPLE_DESC + f" (one pass, {dt:.1f} s)"}
+               "sample": sample_desc(n_rows) + f" (one pass, {dt:.1f} s)"}
         del data
 
     host, d = make_device_data(torch, dev)
@@ -352,14 +383,14 @@ def run_ours(args):
         e2e_ms = a.elapsed_time(b) / n_e2e
         e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    times = torch.tensor([elapsed_ms, e2e["ms_per_step"] if e2e else 0.0], device=dev)
-    if dist:
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    elapsed_ms = float(times[0])
+    elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e["ms_per_step"] if e2e else 0.0], dist,
+                                        dev)
+    if e2e:
+        e2e["ms_per_step"] = e2e_ms
     flops = step_flops()
-    total_flops = sum(flops.values()) * world
     ms_per_step = elapsed_ms / args.steps
-    value = total_flops / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(sum(flops.values()), world, ms_per_step)
+    total_flops = sum(flops.values()) * world
 
     if rank != 0:
         if dist:

@@ -1,12 +1,12 @@
 // Backward exact attention on sm_103a.  Three launches on one stream:
 //
-//  1. bwd_pre     D_i = sum_k dO_ik O_ik (equal to sum_j P_ij dP_ij), LSE in
+//  1. bwd_pre     D_i = sum_k dO_ik O_ik (equal to sum_j P_ij dP_ij), -LSE in
 //                 log2 units, zeroed fp32 dQ accumulator.
 //  2. bwd_main    one CTA per (batch*head, 128-key tile j); loops over query
 //                 tiles i, regenerating P from Q, K and the saved log-sum-exp
 //                 (FlashAttention item 58: backward recomputes score tiles from
 //                 inputs and normalisation statistics):
-//                     S^T  = K Q_i^T            P^T = 2^(S^T*cs - LSE2)
+//                     S^T  = K Q_i^T            P^T = 2^(S^T*cs - LSE*log2(e))
 //                     dP^T = V dO_i^T           dS^T = P^T (dP^T - D)
 //                     dV  += P^T dO_i           dK  += dS^T Q_i
 //                     dQ_i += dS K   (fp32 reductions into the accumulator)
@@ -41,28 +41,34 @@ constexpr float kLog2e = 1.44269504088896340736f;
 
 template <int D>
 struct BwdTraits {
-    static constexpr int NBLK = D / 64;
-    static constexpr int BLK_BYTES = kTile * 128;
+    static constexpr int NBLK = D / 64;                 // 128-byte column blocks of a K/V/Q/dO row
+    static constexpr int NDQ = D / 64;                  // dQ tile computed as NDQ parts of 64 columns
+    static constexpr int BLK_BYTES = kTile * 128;       // one [128 rows x 128 B] block
+    static constexpr int HALF_BYTES = 64 * 128;         // 64 rows of a block (one query half)
     static constexpr int TILE_BYTES = kTile * D * 2;
-    static constexpr int DS_BYTES = kTile * kTile * 2;
+    static constexpr int DS_BYTES = kTile * kTile * 2;  // dS^T [128 keys][128 queries], 2 blocks
     static constexpr int STAGES = 2;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + TILE_BYTES;
     static constexpr int OFF_Q = OFF_V + TILE_BYTES;                 // + stage * TILE_BYTES
     static constexpr int OFF_DO = OFF_Q + STAGES * TILE_BYTES;       // + stage * TILE_BYTES
     static constexpr int OFF_DS = OFF_DO + STAGES * TILE_BYTES;
-    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;                // LSE2[s], D[s]: 512 B each
+    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;                // -LSE2[s], D[s]: 512 B each
     static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * 512;
-    // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full, p_full, dq_full, dq_empty, dkv_full, done
-    static constexpr int NBARS = 1 + 2 * STAGES + 6;
+    // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full[2], p_full[2], dq_full[2],
+    //           dq_empty[2], dkv_full, done
+    static constexpr int NBARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
-    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 256 + D;
-    static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, kTile, false, false);
-    static constexpr uint32_t IDESC_DV = make_idesc(kFmtBF16, kTile, D, false, true);
-    static constexpr uint32_t IDESC_DQ = make_idesc(kFmtBF16, kTile, D, true, true);
-    static constexpr uint32_t IDESC_DK = make_idesc(kFmtBF16, kTile, D, false, true);
+    // Region h (h = query half) = 128 columns: S^T_h at +0, dP^T_h at +64.
+    static constexpr uint32_t COL_REGION = 128, COL_DP = 64;
+    static constexpr uint32_t COL_DV = 256, COL_DK = 256 + D;
+    static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, 64, false, false);
+    static constexpr uint32_t IDESC_DVK = make_idesc(kFmtBF16, kTile, D, false, true);
+    static constexpr uint32_t IDESC_DQ = make_idesc(kFmtBF16, kTile, 64, true, true);
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
+
+constexpr int kBwdThreads = 448;  // 14 warps
 
 enum : uint32_t {
     SITE_KV = 0x201, SITE_QDO_EMPTY = 0x202, SITE_QDO_FULL = 0x203, SITE_DQ_EMPTY = 0x204,
@@ -107,7 +113,7 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
         if (lane == 0) {
             const size_t v = static_cast<size_t>(bh) * p.Npad + n;
             p.dsum[v] = acc;
-            p.lse2[v] = n < p.N ? p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e : INFINITY;
+            p.lse2[v] = n < p.N ? -p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e : -INFINITY;
         }
         float4* z = reinterpret_cast<float4*>(p.dq_acc + r * p.D);
         for (int c = lane; c < p.D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -139,8 +145,12 @@ __global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p
 // ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
+// Each 128-row query tile is processed as two 64-row halves h, each with its
+// own compute warpgroup and its own 128 tensor-memory columns, so that the
+// tensor core computes one half's S^T/dP^T while the other half's P^T/dS^T
+// are being formed, and dV/dK for a half start as soon as that half is ready.
 template <int D>
-__global__ void __launch_bounds__(320, 1)
+__global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                     const BwdParams prm) {
@@ -157,12 +167,12 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t b_kv = bar0;
     auto b_qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
     auto b_qdo_empty = [&](int s) { return bar0 + 8u * (1 + T::STAGES + s); };
-    const uint32_t b_s_full = bar0 + 8u * (1 + 2 * T::STAGES);
-    const uint32_t b_p_full = b_s_full + 8u;
-    const uint32_t b_dq_full = b_s_full + 16u;
-    const uint32_t b_dq_empty = b_s_full + 24u;
-    const uint32_t b_dkv_full = b_s_full + 32u;
-    const uint32_t b_done = b_s_full + 40u;
+    const uint32_t b_s_full = bar0 + 8u * (1 + 2 * T::STAGES);  // + 8*h
+    const uint32_t b_p_full = b_s_full + 16u;                   // + 8*h
+    const uint32_t b_dq_full = b_p_full + 16u;                  // + 8*p
+    const uint32_t b_dq_empty = b_dq_full + 16u;                // + 8*p
+    const uint32_t b_dkv_full = b_dq_empty + 16u;
+    const uint32_t b_done = b_dkv_full + 8u;
 
     if ((sbase & 1023u) != 0) {
         if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FF);
@@ -191,20 +201,22 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(b_qdo_full(s), 1);
             mbar_init(b_qdo_empty(s), 1);
         }
-        mbar_init(b_s_full, 1);
-        mbar_init(b_p_full, 4);
-        mbar_init(b_dq_full, 1);
-        mbar_init(b_dq_empty, 4);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(b_s_full + 8u * h, 1);
+            mbar_init(b_p_full + 8u * h, 4);    // one arrival per compute warp
+            mbar_init(b_dq_full + 8u * h, 1);
+            mbar_init(b_dq_empty + 8u * h, 4);  // one arrival per dQ-writer warp
+        }
         mbar_init(b_dkv_full, 1);
         mbar_init(b_done, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 13) {
         tmem_alloc(smem_u32(tmem_slot), 512);
         tmem_relinquish();
     }
-    if (warp == 8 && lane == 0) {
+    if (warp == 12 && lane == 0) {
         tma_prefetch_map(&tm_q);
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
@@ -217,7 +229,7 @@ __global__ void __launch_bounds__(320, 1)
     const float* lse2_g = prm.lse2 + static_cast<size_t>(bh) * prm.Npad;
     const float* dsum_g = prm.dsum + static_cast<size_t>(bh) * prm.Npad;
 
-    if (warp == 8) {
+    if (warp == 12) {
         // ================= TMA producer =================
         if (lane == 0) {
             mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
@@ -249,10 +261,9 @@ __global__ void __launch_bounds__(320, 1)
             for (int u = first; u < t; ++u)
                 wait_drain(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, prm.st, SITE_DRAIN);
         }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
         // ================= MMA issuer =================
         if (lane == 0) {
-            const uint32_t tS = tmem + T::COL_S, tDP = tmem + T::COL_DP;
             const uint32_t tDV = tmem + T::COL_DV, tDK = tmem + T::COL_DK;
             const uint32_t sK = sbase + T::OFF_K, sV = sbase + T::OFF_V, sDS = sbase + T::OFF_DS;
             // K-major operand, 16 bf16 (32 bytes) of K per instruction.
@@ -272,33 +283,52 @@ __global__ void __launch_bounds__(320, 1)
                     if (!wait_one(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL))
                         return false;
                     tc_fence_after();
+                    for (int h = 0; h < 2; ++h) {
+                        const uint32_t tR = tmem + h * T::COL_REGION;
+                        // S^T_h = K Q_h^T  (M = 128 keys, N = 64 queries, K = d)
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss<false>(tS, kmaj(sK, kk), kmaj(sQ, kk), T::IDESC_SDP, kk > 0);
-                    if (t > 0) {  // dQ_{t-1} must have left the dP^T columns
-                        if (!wait_one(b_dq_empty, (t - 1) & 1, abort_flag, prm.st, SITE_DQ_EMPTY))
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss<false>(tR, kmaj(sK, kk), kmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_SDP,
+                                          kk > 0);
+                        if (t > 0 && h < T::NDQ) {  // dQ part h of the previous tile has left
+                            if (!wait_one(b_dq_empty + 8u * h, (t - 1) & 1, abort_flag, prm.st,
+                                          SITE_DQ_EMPTY))
+                                return false;
+                            tc_fence_after();
+                        }
+                        // dP^T_h = V dO_h^T
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            mma_ss<false>(tR + T::COL_DP, kmaj(sV, kk), kmaj(sDO + h * T::HALF_BYTES, kk),
+                                          T::IDESC_SDP, kk > 0);
+                        mma_commit(b_s_full + 8u * h);
+                    }
+                    for (int h = 0; h < 2; ++h) {
+                        if (!wait_one(b_p_full + 8u * h, t & 1, abort_flag, prm.st, SITE_P_FULL))
                             return false;
                         tc_fence_after();
+                        const uint32_t tR = tmem + h * T::COL_REGION;
+                        // dV += P^T_h dO_h : A = P^T_h (tensor memory), B = dO_h (MN-major)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ts<false>(tDV, tR + kk * 8, mnmaj(sDO + h * T::HALF_BYTES, kk),
+                                          T::IDESC_DVK, (t > 0 || h > 0 || kk > 0));
+                        // dK += dS^T_h Q_h : A = dS^T block h (K-major), B = Q_h (MN-major)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_ss<false>(tDK, kmaj(sDS + h * T::BLK_BYTES, kk),
+                                          mnmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_DVK,
+                                          (t > 0 || h > 0 || kk > 0));
                     }
+                    // dQ_i = dS K, in parts of 64 columns, each into the dP^T columns of region p
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        mma_ss<false>(tDP, kmaj(sV, kk), kmaj(sDO, kk), T::IDESC_SDP, kk > 0);
-                    mma_commit(b_s_full);
-                    if (!wait_one(b_p_full, t & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
-                    tc_fence_after();
-                    // dQ_i = dS K : A = dS (MN-major view of dS^T), B = K (MN-major)
+                    for (int p = 0; p < T::NDQ; ++p) {
 #pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ss<false>(tDP, mnmaj(sDS, kk), mnmaj(sK, kk), T::IDESC_DQ, kk > 0);
-                    mma_commit(b_dq_full);
-                    // dV += P^T dO_i : A = P^T in tensor memory, B = dO_i (MN-major)
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ts<false>(tDV, tS + kk * 8, mnmaj(sDO, kk), T::IDESC_DV, (t > 0 || kk > 0));
-                    // dK += dS^T Q_i : A = dS^T (K-major), B = Q_i (MN-major)
-#pragma unroll
-                    for (int kk = 0; kk < kTile / 16; ++kk)
-                        mma_ss<false>(tDK, kmaj(sDS, kk), mnmaj(sQ, kk), T::IDESC_DK, (t > 0 || kk > 0));
+                        for (int kk = 0; kk < kTile / 16; ++kk)
+                            mma_ss<false>(tmem + p * T::COL_REGION + T::COL_DP, mnmaj(sDS, kk),
+                                          mnmaj(sK + p * T::BLK_BYTES, kk), T::IDESC_DQ, kk > 0);
+                        mma_commit(b_dq_full + 8u * p);
+                    }
                     mma_commit(b_qdo_empty(s));
                 }
                 mma_commit(b_dkv_full);
@@ -308,128 +338,144 @@ __global__ void __launch_bounds__(320, 1)
             mma_commit(b_done);
             wait_drain(b_done, 0, prm.st, SITE_DRAIN);
         }
-    } else if (warp < 4) {
-        // ================= compute warpgroup: P^T, dS^T =================
-        const int r = warp * 32 + lane;  // key row within the tile
+    } else if (warp < 8) {
+        // ================= compute warpgroups: P^T, dS^T for query half h =================
+        const int h = warp >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // key row within the tile
         const int kv_row = j * kTile + r;
-        const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t tS = tmem + T::COL_S + lane_off, tDP = tmem + T::COL_DP + lane_off;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tS = tmem + h * T::COL_REGION + lane_off;
+        const uint32_t tDP = tS + T::COL_DP;
         const float cs = prm.cs;
-        uint8_t* ds_row = smem + T::OFF_DS + r * 128;
+        uint8_t* ds_row = smem + T::OFF_DS + h * T::BLK_BYTES + r * 128;
         const int sw = r & 7;
+        const uint32_t b_sf = b_s_full + 8u * h, b_pf = b_p_full + 8u * h;
         bool ok = true;
         for (int t = 0; t < n_steps; ++t) {
             const int s = t % T::STAGES;
             const int i = q_tile(t);
-            const float* lse2 = reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024);
-            const float* dsum = lse2 + 128;
-            // LSE2_i and D_i arrived with Q_i/dO_i; waiting here (the phase is already
+            const float* nlse2 =
+                reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024) + h * 64;
+            const float* dsum = nlse2 + 128;
+            // -LSE2_i and D_i arrived with Q_i/dO_i; waiting here (the phase is already
             // complete) makes those bulk-copied bytes visible to this thread.
             if (!wait_warp(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL) ||
-                !wait_warp(b_s_full, t & 1, abort_flag, prm.st, SITE_S_FULL)) {
+                !wait_warp(b_sf, t & 1, abort_flag, prm.st, SITE_S_FULL)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
-            // diagonal tile: query column c visible iff c >= r
-            const int cmin = (prm.causal && i == j) ? r : 0;
+            // diagonal tile: query column h*64 + c visible iff h*64 + c >= r
+            const int cmin = (prm.causal && i == j) ? r - h * 64 : 0;
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {  // two halves of 64 query columns
-                uint32_t pk[32];
+            for (int cc = 0; cc < 2; ++cc) {  // two chunks of 32 query columns
+                const int c0 = cc * 32;
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tS + c0, sv);
+                tmem_ld32(tDP + c0, dp);
+                tmem_ld_wait(sv);
+                tmem_ld_wait(dp);
+                uint32_t pk[16], dsw[16];
+                const float4* nl4 = reinterpret_cast<const float4*>(nlse2 + c0);
+                const float4* ds4 = reinterpret_cast<const float4*>(dsum + c0);
 #pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int c0 = h * 64 + cc * 32;
-                    uint32_t sv[32], dp[32];
-                    tmem_ld32(tS + c0, sv);
-                    tmem_ld32(tDP + c0, dp);
-                    tmem_ld_wait(sv);
-                    tmem_ld_wait(dp);
-                    uint32_t dsw[16];
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 nl = nl4[e / 4];  // same address in every lane: broadcast
+                    const float4 dd = ds4[e / 4];
+                    const float nlv[4] = {nl.x, nl.y, nl.z, nl.w};
+                    const float ddv[4] = {dd.x, dd.y, dd.z, dd.w};
 #pragma unroll
-                    for (int e = 0; e < 32; e += 2) {
-                        const int c = c0 + e;
-                        float p0 = ex2_approx(fmaf(u2f(sv[e]), cs, -lse2[c]));
-                        float p1 = ex2_approx(fmaf(u2f(sv[e + 1]), cs, -lse2[c + 1]));
+                    for (int h2 = 0; h2 < 4; h2 += 2) {
+                        const int c = c0 + e + h2;
+                        float x0, x1, t0, t1, d0, d1;
+                        ffma2(x0, x1, u2f(sv[e + h2]), u2f(sv[e + h2 + 1]), cs, cs, nlv[h2], nlv[h2 + 1]);
+                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         if (c < cmin) p0 = 0.f;
                         if (c + 1 < cmin) p1 = 0.f;
-                        pk[cc * 16 + e / 2] = pack_bf16x2(p0, p1);
-                        const float d0 = p0 * (u2f(dp[e]) - dsum[c]);
-                        const float d1 = p1 * (u2f(dp[e + 1]) - dsum[c + 1]);
-                        dsw[e / 2] = pack_bf16x2(d0, d1);
+                        pk[(e + h2) / 2] = pack_bf16x2(p0, p1);
+                        fsub2(t0, t1, u2f(dp[e + h2]), u2f(dp[e + h2 + 1]), ddv[h2], ddv[h2 + 1]);
+                        fmul2(d0, d1, p0, p1, t0, t1);
+                        dsw[(e + h2) / 2] = pack_bf16x2(d0, d1);
                     }
-                    // 64 bytes of dS^T row r -> 16-byte chunks x = (c0 % 64) / 8 .. +3, swizzled
-                    uint8_t* blk = ds_row + (c0 / 64) * T::BLK_BYTES;
-                    const int x0 = (c0 & 63) / 8;
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        *reinterpret_cast<uint4*>(blk + (((x0 + v) ^ sw) << 4)) =
-                            make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3]);
                 }
-                tmem_st32(tS + 32 * h, pk);
+                // P^T chunk -> columns [16 cc, 16 cc + 16) of S^T_h (already read)
+                tmem_st16(tS + 16 * cc, pk);
+                // dS^T row r, 64 bytes -> 16-byte chunks x = 4 cc .. 4 cc + 3, swizzled
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    *reinterpret_cast<uint4*>(ds_row + (((cc * 4 + v) ^ sw) << 4)) =
+                        make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3]);
             }
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(b_p_full);
+            if (lane == 0) mbar_arrive(b_pf);
         }
-        // ---- epilogue: dV, dK (scaled) -> bf16 ----
+        // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled) ----
         if (ok && wait_warp(b_dkv_full, 0, abort_flag, prm.st, SITE_DKV)) {
             tc_fence_after();
             const bool row_ok = kv_row < N;
             const size_t roff = (static_cast<size_t>(bh) * N + (row_ok ? kv_row : 0)) * D * 2;
+            const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
+            uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
+            const float f = h ? prm.scale : 1.f;
 #pragma unroll
-            for (int which = 0; which < 2; ++which) {
-                const uint32_t tsrc = tmem + (which ? T::COL_DK : T::COL_DV) + lane_off;
-                uint8_t* dst = static_cast<uint8_t*>(which ? prm.dk : prm.dv) + roff;
-                const float f = which ? prm.scale : 1.f;
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tsrc + 32 * c, o);
+                tmem_ld_wait(o);
+                uint32_t pk[16];
 #pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    uint32_t o[32];
-                    tmem_ld32(tsrc + 32 * c, o);
-                    tmem_ld_wait(o);
-                    uint32_t pk[16];
+                for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f);
+                if (row_ok) {
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f);
-                    if (row_ok) {
-#pragma unroll
-                        for (int v = 0; v < 4; ++v)
-                            st_global_v4(dst + c * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
-                                         pk[4 * v + 3]);
-                    }
+                    for (int v = 0; v < 4; ++v)
+                        st_global_v4(dst + c * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                     pk[4 * v + 3]);
                 }
             }
         }
     } else {
-        // ================= dQ writer warpgroup =================
+        // ================= dQ writer warpgroup (warps 8-11) =================
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // query row within tile i
-        const uint32_t tDQ = tmem + T::COL_DP + (static_cast<uint32_t>(wq * 32) << 16);
-        for (int t = 0; t < n_steps; ++t) {
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        bool ok = true;
+        for (int t = 0; t < n_steps && ok; ++t) {
             const int i = q_tile(t);
-            if (!wait_warp(b_dq_full, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) break;
-            tc_fence_after();
             float* dst = prm.dq_acc + (static_cast<size_t>(bh) * prm.Npad + i * kTile + r) * D;
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld32(tDQ + 32 * c, v);
-                tmem_ld_wait(v);
-                if (c == D / 32 - 1) {  // the tile has left tensor memory
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_dq_empty);
+            for (int p = 0; p < T::NDQ; ++p) {
+                if (!wait_warp(b_dq_full + 8u * p, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
+                    ok = false;
+                    break;
                 }
+                tc_fence_after();
+                const uint32_t tq = tmem + p * T::COL_REGION + T::COL_DP + lane_off;
+                uint32_t v0[32], v1[32];
+                tmem_ld32(tq, v0);
+                tmem_ld32(tq + 32, v1);
+                tmem_ld_wait(v0);
+                tmem_ld_wait(v1);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_dq_empty + 8u * p);  // part p has left tensor memory
 #pragma unroll
                 for (int e = 0; e < 32; e += 4)
-                    red_add_v4(dst + c * 32 + e, u2f(v[e]), u2f(v[e + 1]), u2f(v[e + 2]), u2f(v[e + 3]));
+                    red_add_v4(dst + p * 64 + e, u2f(v0[e]), u2f(v0[e + 1]), u2f(v0[e + 2]), u2f(v0[e + 3]));
+#pragma unroll
+                for (int e = 0; e < 32; e += 4)
+                    red_add_v4(dst + p * 64 + 32 + e, u2f(v1[e]), u2f(v1[e + 1]), u2f(v1[e + 2]),
+                               u2f(v1[e + 3]));
             }
         }
     }
 
     tc_fence_before();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 13) {
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
@@ -443,7 +489,7 @@ cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, c
         bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     const long long grid = static_cast<long long>(p.BH) * p.n_kv;
-    bwd_main_kernel<D><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
+    bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
     return cudaGetLastError();
 }
 

@@ -312,9 +312,10 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-                for (int i = 0; i < 32; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], u2f(s[c][i]));
-            const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                   fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+                for (int i = (c == 0 ? 8 : 0); i < 32; i += 2)
+                    mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], u2f(s[c][i]), u2f(s[c][i + 1]));
+            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                   fmaxf(mx8[6], mx8[7]));
             const float mx_s = mx * cs;
 
             float alpha = 1.f;
@@ -354,12 +355,12 @@ __global__ void __launch_bounds__(320, 1)
                         const int c = 2 * h + cc;
 #pragma unroll
                         for (int i = 0; i < 32; i += 2) {
-                            const float p0 = ex2_approx(fmaf(u2f(s[c][i]), cs, -m_sub));
-                            const float p1 = ex2_approx(fmaf(u2f(s[c][i + 1]), cs, -m_sub));
-                            const uint32_t w = pack_bf16x2(p0, p1);
+                            float x0, x1;
+                            ffma2(x0, x1, u2f(s[c][i]), u2f(s[c][i + 1]), cs, cs, -m_sub, -m_sub);
+                            const uint32_t w = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
                             // The normaliser sums the same bf16 values that multiply V, so
                             // O stays an exact convex combination of V rows.
-                            ls[(i >> 1) & 3] += __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+                            ls[(i >> 1) & 3] = add_bf16x2(ls[(i >> 1) & 3], w);
                             pk[cc * 16 + i / 2] = w;
                         }
                     }

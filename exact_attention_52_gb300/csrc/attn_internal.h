@@ -28,13 +28,13 @@ struct BwdPreParams {
     const void* dout;  // bf16 [BH, N, D]
     const float* lse;  // fp32 [BH, N]
     float* dq_acc;     // fp32 [BH, Npad, D], zeroed here
-    float* lse2;       // fp32 [BH, Npad]: LSE * log2(e); +inf on padding rows
+    float* lse2;       // fp32 [BH, Npad]: -LSE * log2(e); -inf on padding rows
     float* dsum;       // fp32 [BH, Npad]: D_i = sum_k dO_ik O_ik; 0 on padding rows
     int N, Npad, BH, D;
 };
 
 struct BwdParams {
-    const float* lse2;  // workspace, see BwdPreParams
+    const float* lse2;  // workspace (-LSE * log2(e)), see BwdPreParams
     const float* dsum;
     float* dq_acc;
     void* dk;           // bf16 [BH, N, D]
