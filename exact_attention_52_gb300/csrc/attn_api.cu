@@ -8,7 +8,7 @@
 #include <cstdint>
 #include <mutex>
 
-#include "../../include/attn_sm103a.h"
+#include "attn_sm103a.h"
 #include "attn_internal.h"
 #include "ptx.cuh"
 

@@ -180,11 +180,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 
     const int N = prm.N;
-    // Head-major order keeps the resident CTAs on a few heads, so those heads'
-    // Q, dO and fp32 dQ accumulator stay in L2 while every key tile reduces
-    // into them.  Within a head, low key tiles (longest causal loops) first.
-    const int bh = static_cast<int>(blockIdx.x / prm.n_kv);
-    const int j = static_cast<int>(blockIdx.x % prm.n_kv);  // key tile
+    // Non-causal: head-major order keeps the resident CTAs on a few heads, so
+    // those heads' Q, dO and fp32 dQ accumulator stay in L2 while every key
+    // tile reduces into them.  Causal: low key tiles (longest loops) of every
+    // head first, which keeps the tail of the launch short.
+    const int bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BH)
+                              : static_cast<int>(blockIdx.x / prm.n_kv);
+    const int j = prm.causal ? static_cast<int>(blockIdx.x / prm.BH)
+                             : static_cast<int>(blockIdx.x % prm.n_kv);  // key tile
     const int n_q_total = (N + kTile - 1) / kTile;
     const int n_steps = prm.causal ? n_q_total - j : n_q_total;
     // Query tile of step t.  Causal: the diagonal tile j, then upwards.

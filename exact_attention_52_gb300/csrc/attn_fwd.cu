@@ -104,11 +104,15 @@ __global__ void __launch_bounds__(320, 1)
     }
 
     // ---- work assignment ----
-    // Head-major order: the CTAs resident at any time cover only a few heads,
-    // so each head's K and V are read from HBM about once and then hit L2.
-    // Within a head the heaviest causal tiles come first.
-    const int bh = static_cast<int>(blockIdx.x / prm.n_pairs);
-    const int pair = prm.n_pairs - 1 - static_cast<int>(blockIdx.x % prm.n_pairs);
+    // Non-causal: head-major order, so the CTAs resident at any time cover
+    // only a few heads and each head's K and V come from HBM about once.
+    // Causal: heaviest query tiles of every head first (longest-first keeps
+    // the tail of the launch short; a causal head needs half the K/V reuse).
+    const int bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BH)
+                              : static_cast<int>(blockIdx.x / prm.n_pairs);
+    const int pair = prm.n_pairs - 1 -
+                     (prm.causal ? static_cast<int>(blockIdx.x / prm.BH)
+                                 : static_cast<int>(blockIdx.x % prm.n_pairs));
     const int N = prm.N;
     const int n_kv_total = (N + kTile - 1) / kTile;
     int n_t[2];
@@ -284,7 +288,8 @@ __global__ void __launch_bounds__(320, 1)
         const int row_limit = prm.causal ? min(N, q_row + 1) : N;  // keys [0, row_limit) visible
 
         float m_used = -INFINITY;  // running max in log2 units of the scaled scores
-        float l_sum = 0.f;         // running sum of 2^(s*cs - m_used)
+        float l_sum = 0.f;         // running sum of 2^(s*cs - m_used), unrounded (for LSE)
+        float l_pv = 0.f;          // the same sum over the rounded P that multiplies V
         bool ok = true;
         for (int j = 0; j < n; ++j) {
             if (!wait_warp(b_sf, j & 1, abort_flag, prm.st, SITE_S_FULL)) {
@@ -323,12 +328,14 @@ __global__ void __launch_bounds__(320, 1)
             if (mx_s > m_used + kRescaleThreshold) {
                 alpha = ex2_approx(m_used - mx_s);  // 0 when m_used is still -inf
                 l_sum *= alpha;
+                l_pv *= alpha;
                 m_used = mx_s;
                 rescale_o = (j > 0);
             }
             const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
 
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
+            float lr[4] = {0.f, 0.f, 0.f, 0.f};
             if constexpr (FP8) {
                 uint32_t pk[32];
 #pragma unroll
@@ -354,20 +361,31 @@ __global__ void __launch_bounds__(320, 1)
                     for (int cc = 0; cc < 2; ++cc) {
                         const int c = 2 * h + cc;
 #pragma unroll
-                        for (int i = 0; i < 32; i += 2) {
-                            float x0, x1;
+                        for (int i = 0; i < 32; i += 4) {
+                            float x0, x1, x2, x3;
                             ffma2(x0, x1, u2f(s[c][i]), u2f(s[c][i + 1]), cs, cs, -m_sub, -m_sub);
-                            const uint32_t w = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
-                            // The normaliser sums the same bf16 values that multiply V, so
-                            // O stays an exact convex combination of V rows.
-                            ls[(i >> 1) & 3] = add_bf16x2(ls[(i >> 1) & 3], w);
-                            pk[cc * 16 + i / 2] = w;
+                            ffma2(x2, x3, u2f(s[c][i + 2]), u2f(s[c][i + 3]), cs, cs, -m_sub, -m_sub);
+                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                            const uint32_t w0 = pack_bf16x2(p0, p1), w1 = pack_bf16x2(p2, p3);
+                            // The O normaliser sums the same bf16 values that multiply V, so
+                            // O stays an exact convex combination of V rows; LSE uses the
+                            // unrounded sum.
+                            lr[(i >> 2) & 1] = add_bf16x2(lr[(i >> 2) & 1], w0);
+                            lr[2 + ((i >> 2) & 1)] = add_bf16x2(lr[2 + ((i >> 2) & 1)], w1);
+                            float a0, a1;
+                            fadd2(a0, a1, p0, p1, p2, p3);
+                            fadd2(ls[(i >> 2) & 1], ls[2 + ((i >> 2) & 1)], ls[(i >> 2) & 1],
+                                  ls[2 + ((i >> 2) & 1)], a0, a1);
+                            pk[cc * 16 + i / 2] = w0;
+                            pk[cc * 16 + i / 2 + 1] = w1;
                         }
                     }
                     tmem_st32(tS + 32 * h, pk);
                 }
             }
             l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
+            l_pv += (lr[0] + lr[1]) + (lr[2] + lr[3]);
             if (__any_sync(0xffffffffu, rescale_o)) {
                 // Rescale this warp's 32 output rows (alpha = 1 on rows that kept their max).
                 // PV_g(j-1) has completed: S_g(j) was committed after it, and PV_g(j)
@@ -392,7 +410,8 @@ __global__ void __launch_bounds__(320, 1)
         if (ok && n > 0 && wait_warp(b_of, 0, abort_flag, prm.st, SITE_O_FULL)) {
             tc_fence_after();
             const bool row_ok = q_row < N;
-            const float inv_l = l_sum > 0.f ? prm.out_scale / l_sum : 0.f;
+            const float l_norm = FP8 ? l_sum : l_pv;
+            const float inv_l = l_norm > 0.f ? prm.out_scale / l_norm : 0.f;
             uint8_t* orow = static_cast<uint8_t*>(prm.o) +
                             (static_cast<size_t>(bh) * N + (row_ok ? q_row : 0)) * D * 2;
 #pragma unroll
