@@ -29,6 +29,8 @@ SIGNATURES = {
     "attn_bwd_preprocess": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp]),
     "attn_bwd_main": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
+    "attn_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
+                              _vp]),
     "attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_check_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),

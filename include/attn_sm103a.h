@@ -116,6 +116,30 @@ attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, 
                                 attn_stream_t stream);
 
 /*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory -- for example code that a host framework hands only its
+ * input and output tensors while the framework owns all device memory and
+ * allows no allocation after start-up.  The pages describe no such variant;
+ * it has no counterpart there.
+ *   Arguments, results and errors are those of attn_bwd, with the scratch
+ *   taken from a fixed 64 MiB array inside the library instead of
+ *   `workspace`.  Problems whose attn_bwd_workspace_bytes() exceeds 64 MiB
+ *   are rejected with ATTN_ERR_UNSUPPORTED before anything is launched
+ *   (about 129k padded rows at d = 128, e.g. B*H*ceil(N/128)*128 <= 129,000).
+ *   The first call on a device looks up the array's device address once
+ *   (with that device current); make that first call before any stream
+ *   capture.  Every GPU that loads this part of the library keeps the 64 MiB
+ *   until the process exits.  Nothing is allocated by any call.
+ *   All calls on a device share the one array: calls that overlap on the GPU
+ *   (unordered streams) race and give wrong results.  Each call zeroes the
+ *   part that must start at zero, so earlier calls do not leak into later ones.
+ */
+attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const void* o,
+                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                             int B, int H, int N, int d, float scale, int causal,
+                             attn_stream_t stream);
+
+/*
  * FP8 forward pass: OCP E4M3 inputs with per-tensor fp32 scales.
  *   q8, k8, v8 : uint8 E4M3 codes [B, H, N, d]; the value read is s * code
  *                (sq, sk, sv finite and > 0).
