@@ -5,8 +5,8 @@ import numpy as np
 
 import oracle
 
-# Tolerances the parity tests enforce (bf16 O max-abs, LSE absolute, gradient
-# relative Frobenius, FP8 O relative Frobenius).
+# Tolerances the parity tests enforce (bf16 O max-abs beyond the output's own
+# rounding, LSE absolute, gradient relative Frobenius, FP8 O relative Frobenius).
 TOL_O_MAXABS = 1e-2
 TOL_LSE_ABS = 1e-3
 TOL_GRAD_RELFRO = 2e-2
@@ -17,6 +17,24 @@ def max_abs(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     return float(np.max(np.abs(a - b))) if a.size else 0.0
+
+
+def bf16_half_ulp(x):
+    """Half the spacing of bfloat16 numbers at |x| (8 significant bits)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, 0.5 * 2.0 ** (e - 7), 0.0)
+
+
+def bf16_out_err(gpu, ref):
+    """Max over elements of |gpu - ref| beyond the rounding of ref itself to
+    bfloat16: the part of the error the computation adds on top of storing the
+    exact result in the output format."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if not gpu.size:
+        return 0.0
+    return float(np.max(np.abs(gpu - ref) - bf16_half_ulp(ref)))
 
 
 def rel_fro(a, b):

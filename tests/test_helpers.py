@@ -1,0 +1,25 @@
+"""The comparison helpers used by the parity tests, checked against PyTorch's
+own bfloat16 rounding (CPU only)."""
+
+import numpy as np
+import pytest
+
+from .helpers import bf16_half_ulp, bf16_out_err, max_abs, rel_fro
+
+
+def test_bf16_half_ulp_bounds_round_to_nearest():
+    torch = pytest.importorskip("torch")
+    x32 = (np.random.Generator(np.random.PCG64(0)).standard_normal(100000) * 3.0).astype(np.float32)
+    x = x32.astype(np.float64)  # single rounding float32 -> bf16 below
+    xb = torch.from_numpy(x32).to(torch.bfloat16).double().numpy()
+    assert np.all(np.abs(xb - x) <= bf16_half_ulp(x) * (1 + 1e-12))
+    assert bf16_out_err(xb, x) <= 1e-12
+    # one spacing off is an error of about half a spacing beyond rounding
+    assert bf16_out_err(np.array([4.0 + 2 ** -5]), np.array([4.0])) == pytest.approx(2 ** -6)
+    assert bf16_half_ulp(np.array([1.0, 4.13, 0.0])).tolist() == [2 ** -8, 2 ** -6, 0.0]
+
+
+def test_metrics():
+    a = np.array([1.0, 2.0, 3.0])
+    assert max_abs(a, a + [0, 0.5, 0]) == 0.5
+    assert rel_fro(a * 1.01, a) == pytest.approx(0.01)
