@@ -100,6 +100,22 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int BH) 
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D view {d, Npad, B*H} of the fp32 dQ accumulator; box {32, 128, 1}
+// (128 bytes x 128 rows), 128-byte swizzle, used for TMA reductions.
+bool make_map_acc(CUtensorMap* m, const float* base, int d, int Npad, int BH) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Npad),
+                                static_cast<cuuint64_t>(BH)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
+                                   static_cast<cuuint64_t>(Npad) * d * 4};
+    const cuuint32_t box[3] = {32u, 128u, 1u};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 constexpr long long kMaxElems = (1ll << 40);  // keeps every byte offset well inside 64 bits
@@ -293,9 +309,10 @@ attn_status attn_bwd_main(const void* q, const void* k, const void* v, const voi
     BwdCall c;
     attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, causal, &c);
     if (rc != ATTN_OK) return rc;
-    CUtensorMap tq, tk, tv, tdo;
+    CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_map(&tq, q, false, d, N, c.BH) || !make_map(&tk, k, false, d, N, c.BH) ||
-        !make_map(&tv, v, false, d, N, c.BH) || !make_map(&tdo, dout, false, d, N, c.BH))
+        !make_map(&tv, v, false, d, N, c.BH) || !make_map(&tdo, dout, false, d, N, c.BH) ||
+        !make_map_acc(&tdq, c.dq_acc, d, c.Np, c.BH))
         return ATTN_ERR_CUDA;
     BwdParams bp;
     bp.lse2 = c.lse2;
@@ -311,7 +328,7 @@ attn_status attn_bwd_main(const void* q, const void* k, const void* v, const voi
     bp.cs = scale * 1.44269504088896340736f;
     bp.scale = scale;
     bp.st = dev_status(c.ds);
-    return launch_bwd_main(d, tq, tk, tv, tdo, bp, reinterpret_cast<cudaStream_t>(stream)) ==
+    return launch_bwd_main(d, tq, tk, tv, tdo, tdq, bp, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
                ? ATTN_OK
                : ATTN_ERR_CUDA;

@@ -56,8 +56,8 @@ struct BwdTraits {
     static constexpr int OFF_VEC = OFF_DS + DS_BYTES;                // -LSE2[s], D[s]: 512 B each
     static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * 512;
     // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full[2], p_full[2], dq_full[2],
-    //           dq_empty[2], dkv_full, done
-    static constexpr int NBARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2;
+    //           dq_empty[2], dkv_full, done, dq_staged[2]
+    static constexpr int NBARS = 1 + 2 * STAGES + 2 + 2 + 2 + 2 + 2 + 2;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
     // Region h (h = query half) = 128 columns: S^T_h at +0, dP^T_h at +64.
     static constexpr uint32_t COL_REGION = 128, COL_DP = 64;
@@ -73,7 +73,7 @@ constexpr int kBwdThreads = 448;  // 14 warps
 enum : uint32_t {
     SITE_KV = 0x201, SITE_QDO_EMPTY = 0x202, SITE_QDO_FULL = 0x203, SITE_DQ_EMPTY = 0x204,
     SITE_P_FULL = 0x205, SITE_S_FULL = 0x206, SITE_DQ_FULL = 0x207, SITE_DKV = 0x208,
-    SITE_DRAIN = 0x209,
+    SITE_DRAIN = 0x209, SITE_DQ_STAGED = 0x20A,
 };
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
@@ -153,7 +153,7 @@ template <int D>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                    const BwdParams prm) {
+                    const __grid_constant__ CUtensorMap tm_dq, const BwdParams prm) {
     using T = BwdTraits<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
@@ -173,6 +173,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t b_dq_empty = b_dq_full + 16u;                // + 8*p
     const uint32_t b_dkv_full = b_dq_empty + 16u;
     const uint32_t b_done = b_dkv_full + 8u;
+    const uint32_t b_dq_staged = b_done + 8u;  // + 8*p: all writer warps staged part p
 
     if ((sbase & 1023u) != 0) {
         if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FF);
@@ -202,13 +203,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(b_kv, 1);
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(b_qdo_full(s), 1);
-            mbar_init(b_qdo_empty(s), 1);
+            mbar_init(b_qdo_empty(s), 2);  // MMA commit + dQ writer (its reductions read the stage)
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(b_s_full + 8u * h, 1);
             mbar_init(b_p_full + 8u * h, 4);    // one arrival per compute warp
             mbar_init(b_dq_full + 8u * h, 1);
             mbar_init(b_dq_empty + 8u * h, 4);  // one arrival per dQ-writer warp
+            mbar_init(b_dq_staged + 8u * h, 4);
         }
         mbar_init(b_dkv_full, 1);
         mbar_init(b_done, 1);
@@ -224,6 +226,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_prefetch_map(&tm_k);
         tma_prefetch_map(&tm_v);
         tma_prefetch_map(&tm_do);
+        tma_prefetch_map(&tm_dq);
     }
     tc_fence_before();
     __syncthreads();
@@ -442,13 +445,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else {
         // ================= dQ writer warpgroup (warps 8-11) =================
+        // Each 64-column dQ part leaves tensor memory into shared memory (the Q
+        // and dO buffers of the stage, free once this tile's MMAs are done), in
+        // the 128-byte swizzled layout of two [128 x 32] fp32 boxes, and one
+        // thread adds the boxes into the fp32 accumulator with TMA reductions.
+        // The stage goes back to the producer when those reductions have read it.
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // query row within tile i
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const bool leader = (warp == 8 && lane == 0);
+        constexpr int SLOTS_PER_BUF = T::TILE_BYTES / (kTile * 128);  // 16 KB boxes per buffer
         bool ok = true;
         for (int t = 0; t < n_steps && ok; ++t) {
+            const int s = t % T::STAGES;
             const int i = q_tile(t);
-            float* dst = prm.dq_acc + (static_cast<size_t>(bh) * prm.Npad + i * kTile + r) * D;
 #pragma unroll
             for (int p = 0; p < T::NDQ; ++p) {
                 if (!wait_warp(b_dq_full + 8u * p, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
@@ -466,14 +476,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_dq_empty + 8u * p);  // part p has left tensor memory
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    red_add_v4(dst + p * 64 + e, u2f(v0[e]), u2f(v0[e + 1]), u2f(v0[e + 2]), u2f(v0[e + 3]));
+                for (int b = 0; b < 2; ++b) {
+                    const int u = 2 * p + b;  // staging box
+                    const uint32_t box = sbase +
+                                         (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
+                                                            : T::OFF_DO + s * T::TILE_BYTES +
+                                                                  (u - SLOTS_PER_BUF) * 16384);
+                    uint8_t* row = smem + (box - sbase) + r * 128;
+                    const uint32_t(&v)[32] = b ? v1 : v0;
 #pragma unroll
-                for (int e = 0; e < 32; e += 4)
-                    red_add_v4(dst + p * 64 + 32 + e, u2f(v1[e]), u2f(v1[e + 1]), u2f(v1[e + 2]),
-                               u2f(v1[e + 3]));
+                    for (int x = 0; x < 8; ++x)
+                        *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) << 4)) =
+                            make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_dq_staged + 8u * p);
+                if (warp == 8) {
+                    // Every writer warp has staged its rows.  A bounded wait, never a bare
+                    // bar.sync: a warp that gave up must not strand the others.  The
+                    // outcome is made uniform across warp 8 before anyone acts on it.
+                    bool staged = true;
+                    if (lane == 0)
+                        staged = wait_one(b_dq_staged + 8u * p, t & 1, abort_flag, prm.st,
+                                          SITE_DQ_STAGED);
+                    if (!__shfl_sync(0xffffffffu, staged ? 1 : 0, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (leader) {
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        const int u = 2 * p + b;
+                        const uint32_t box = sbase +
+                                             (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
+                                                                : T::OFF_DO + s * T::TILE_BYTES +
+                                                                      (u - SLOTS_PER_BUF) * 16384);
+                        tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
+                    }
+                    bulk_commit_group();
+                }
+            }
+            if (!ok) break;
+            if (leader) {
+                bulk_wait_group_read0();       // the stage's bytes have been read
+                mbar_arrive(b_qdo_empty(s));   // second arrival: the producer may refill it
             }
         }
+        if (leader) bulk_wait_group0();  // every reduction has landed before the CTA retires
     }
 
     tc_fence_before();
@@ -486,13 +537,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
 template <int D>
 cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                                 const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
+                                 const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                                 cudaStream_t stream) {
     using T = BwdTraits<D>;
     static const cudaError_t attr = cudaFuncSetAttribute(
         bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     const long long grid = static_cast<long long>(p.BH) * p.n_kv;
-    bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, p);
+    bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq,
+                                                                                        p);
     return cudaGetLastError();
 }
 
@@ -515,9 +568,10 @@ cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
 }
 
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, cudaStream_t stream) {
-    if (D == 64) return launch_bwd_main_impl<64>(tq, tk, tv, tdo, p, stream);
-    if (D == 128) return launch_bwd_main_impl<128>(tq, tk, tv, tdo, p, stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
+                            cudaStream_t stream) {
+    if (D == 64) return launch_bwd_main_impl<64>(tq, tk, tv, tdo, tdq, p, stream);
+    if (D == 128) return launch_bwd_main_impl<128>(tq, tk, tv, tdo, tdq, p, stream);
     return cudaErrorInvalidValue;
 }
 

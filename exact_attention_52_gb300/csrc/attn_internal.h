@@ -61,8 +61,8 @@ cudaError_t launch_fwd_fp8(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
-                            cudaStream_t stream);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
+                            const BwdParams& p, cudaStream_t stream);
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream);
 
