@@ -426,7 +426,7 @@ def run_ours(args):
                      "frac": round(achieved / sustained, 4),
                      "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
                      "traffic": traffic,
-                     "algorithmic_bytes": attn_bytes(B, H, N, D, "bwd")},
+                     "algorithmic_bytes": attn_bytes(B, H, N, D, "bwd_main")},
         "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,

@@ -13,6 +13,9 @@ Algorithmic HBM bytes: what one pass must move at least once.
   backward    : read Q, K, V, O, dO, write dQ, dK, dV (2 B each), read LSE
                 and D, plus the fp32 dQ accumulator written once and read
                 once (4 + 4 B/elem).
+  backward main kernel alone: read Q, K, V, dO (2 B each), write dK, dV
+                (2 B each), read LSE and D (4 B/row each), and read + write
+                the fp32 dQ accumulator once (8 B/elem).
 """
 
 from __future__ import annotations
@@ -36,4 +39,6 @@ def attn_bytes(B: int, H: int, N: int, d: int, pass_: str = "fwd") -> float:
         return 5.0 * elems + 4.0 * rows
     if pass_ == "bwd":
         return 16.0 * elems + 8.0 * elems + 8.0 * rows
+    if pass_ == "bwd_main":
+        return 12.0 * elems + 8.0 * elems + 8.0 * rows
     raise ValueError(pass_)
