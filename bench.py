@@ -442,6 +442,76 @@ def run_ours(args):
     return 0
 
 
+EXTRA_WORKLOADS = {
+    # grouped-query attention, 4 query heads per key/value head
+    "gqa_b1_h32_hk8_n8192_d128": dict(B=1, H=32, Hk=8, N=8192, d=128, causal=False),
+    "gqa_causal_b2_h32_hk4_n4096_d128": dict(B=2, H=32, Hk=4, N=4096, d=128, causal=True),
+    "mqa_b4_h16_hk1_n4096_d128": dict(B=4, H=16, Hk=1, N=4096, d=128, causal=False),
+}
+
+
+def run_extra(args):
+    """Forward + backward on one of EXTRA_WORKLOADS (a secondary measurement of
+    the grouped-query path; the default run measures the main step)."""
+    import torch
+
+    from exact_attention_52_gb300 import api
+    from exact_attention_52_gb300.inputs import make_inputs_gqa
+
+    w = EXTRA_WORKLOADS[args.workload]
+    B, H, Hk, N, D, causal = w["B"], w["H"], w["Hk"], w["N"], w["d"], w["causal"]
+    torch.cuda.set_device(0)
+    inp = make_inputs_gqa(B, H, Hk, N, D, seed=0, with_grad=True)
+    import numpy as np
+
+    def dev(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
+
+    q, k, v, do = (dev(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    o = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws = torch.empty(api.bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        api.fwd(q, k, v, causal=causal, o=o, lse=lse)
+        if ev:
+            ev[1].record(stream)
+        api.bwd(q, k, v, o, do, lse, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    rc, site = api.check_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} at wait site {site:#x}")
+    steps = min(args.steps, 50)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        step(evs[i])
+    torch.cuda.synchronize()
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    f = attn_flops(B, H, N, D, causal)
+    peaks, kind = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
+            "value": round(3.5 * f / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+            "components": {
+                "fwd": {"ms": round(fwd_ms, 4), "tflops": round(f / (fwd_ms * 1e-3) / 1e12, 1),
+                        "frac_of_burst": round(f / (fwd_ms * 1e-3) / 1e12 / burst, 4)},
+                "bwd": {"ms": round(bwd_ms, 4), "tflops": round(2.5 * f / (bwd_ms * 1e-3) / 1e12, 1),
+                        "frac_of_burst": round(2.5 * f / (bwd_ms * 1e-3) / 1e12 / burst, 4)}},
+            "peak_kind": kind, "dtype": "bf16", "data": "synthetic"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -451,7 +521,11 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (used for profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--workload", choices=("main",) + tuple(EXTRA_WORKLOADS), default="main",
+                    help="secondary workloads print their own line (not the benchmark step)")
     args = ap.parse_args()
+    if args.workload != "main" and args.impl == "ours":
+        return run_extra(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

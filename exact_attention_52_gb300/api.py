@@ -31,6 +31,9 @@ SIGNATURES = {
     "attn_bwd_dq_convert": (_i, [_vp, _vp, _i, _i, _i, _i, _f, _vp]),
     "attn_bwd_noalloc": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i,
                               _vp]),
+    "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
+    "attn_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
+                          _i, _vp]),
     "attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_check_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
@@ -94,8 +97,10 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, o=None, lse=N
     """Forward pass on bf16 CUDA tensors [B, H, N, d]; returns (O bf16, LSE fp32 [B, H, N])."""
     import torch
     B, H, N, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v)):
-        _check_qkv(name, t, (B, H, N, d), torch.bfloat16)
+    Hk = k.shape[1] if getattr(k, "dim", lambda: 0)() == 4 else H
+    _check_qkv("q", q, (B, H, N, d), torch.bfloat16)
+    for name, t in (("k", k), ("v", v)):
+        _check_qkv(name, t, (B, Hk, N, d), torch.bfloat16)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     if o is None:
         o = torch.empty_like(q)
@@ -104,9 +109,14 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, o=None, lse=N
     _check_qkv("o", o, (B, H, N, d), torch.bfloat16)
     _check_qkv("lse", lse, (B, H, N), torch.float32)
     lib = load_library()
-    _check("attn_fwd", lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                    lse.data_ptr(), B, H, N, d, scale, int(bool(causal)),
-                                    _stream_handle(stream)))
+    if Hk == H:
+        _check("attn_fwd", lib.attn_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        lse.data_ptr(), B, H, N, d, scale, int(bool(causal)),
+                                        _stream_handle(stream)))
+    else:
+        _check("attn_fwd_gqa", lib.attn_fwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                o.data_ptr(), lse.data_ptr(), B, H, Hk, N, d, scale,
+                                                int(bool(causal)), _stream_handle(stream)))
     return o, lse
 
 
@@ -119,25 +129,36 @@ def bwd(q, k, v, o, dout, lse, scale: float | None = None, causal: bool = False,
     """Backward pass; returns (dQ, dK, dV) bf16 [B, H, N, d]."""
     import torch
     B, H, N, d = q.shape
-    for name, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+    Hk = k.shape[1] if getattr(k, "dim", lambda: 0)() == 4 else H
+    for name, t in (("q", q), ("o", o), ("dout", dout)):
         _check_qkv(name, t, (B, H, N, d), torch.bfloat16)
+    for name, t in (("k", k), ("v", v)):
+        _check_qkv(name, t, (B, Hk, N, d), torch.bfloat16)
     _check_qkv("lse", lse, (B, H, N), torch.float32)
     scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
-    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
-        _check_qkv(name, t, (B, H, N, d), torch.bfloat16)
+    _check_qkv("dq", dq, (B, H, N, d), torch.bfloat16)
+    for name, t in (("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, Hk, N, d), torch.bfloat16)
     need = bwd_workspace_bytes(B, H, N, d)
     if workspace is None:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
     if workspace.numel() * workspace.element_size() < need:
         raise ValueError(f"workspace needs {need} bytes")
     lib = load_library()
-    _check("attn_bwd", lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
-                                    dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
-                                    dv.data_ptr(), workspace.data_ptr(), B, H, N, d, scale,
-                                    int(bool(causal)), _stream_handle(stream)))
+    if Hk == H:
+        _check("attn_bwd", lib.attn_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                                        dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                                        dv.data_ptr(), workspace.data_ptr(), B, H, N, d, scale,
+                                        int(bool(causal)), _stream_handle(stream)))
+    else:
+        _check("attn_bwd_gqa", lib.attn_bwd_gqa(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+                                                dq.data_ptr(), dk.data_ptr(), dv.data_ptr(),
+                                                workspace.data_ptr(), B, H, Hk, N, d, scale,
+                                                int(bool(causal)), _stream_handle(stream)))
     return dq, dk, dv
 
 

@@ -184,24 +184,31 @@ using namespace attn;
 
 extern "C" {
 
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                     int N, int d, float scale, int causal, attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                       int Hk, int N, int d, float scale, int causal, attn_stream_t stream) {
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
+    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_INVALID;
     DeviceState* ds = nullptr;
     if ((rc = device_state(&ds)) != ATTN_OK) return rc;
     const int BH = B * H;
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, BH) ||
-        !make_map(&tv, v, false, d, N, BH))
+    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, B * Hk) ||
+        !make_map(&tv, v, false, d, N, B * Hk))
         return ATTN_ERR_CUDA;
     FwdParams p;
     p.o = o;
     p.lse = lse;
     p.N = N;
     p.BH = BH;
+    p.H = H;
+    p.Hk = Hk;
     p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
     p.causal = causal;
     p.cs = scale * 1.44269504088896340736f;
@@ -210,6 +217,20 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
     return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
                : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, float scale, int causal, attn_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
+}
+
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hk, int N, int d, float scale, int causal, attn_stream_t stream) {
+    return fwd_common(q, k, v, o, lse, B, H, Hk, N, d, scale, causal, stream);
 }
 
 attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float sq, float sk, float sv,
@@ -234,6 +255,8 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
     p.lse = lse;
     p.N = N;
     p.BH = BH;
+    p.H = H;
+    p.Hk = H;
     p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
     p.causal = causal;
     p.cs = scale * sq * sk * 1.44269504088896340736f;
@@ -301,17 +324,22 @@ attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* ls
                                                                                      : ATTN_ERR_CUDA;
 }
 
-attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
-                          void* dv, void* workspace, int B, int H, int N, int d, float scale,
-                          int causal, attn_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status bwd_main_common(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                            void* dv, void* workspace, int B, int H, int Hk, int N, int d, float scale,
+                            int causal, attn_stream_t stream) {
     for (const void* p : {q, k, v, dout, static_cast<const void*>(dk), static_cast<const void*>(dv)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
+    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
     BwdCall c;
     attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, causal, &c);
     if (rc != ATTN_OK) return rc;
     CUtensorMap tq, tk, tv, tdo, tdq;
-    if (!make_map(&tq, q, false, d, N, c.BH) || !make_map(&tk, k, false, d, N, c.BH) ||
-        !make_map(&tv, v, false, d, N, c.BH) || !make_map(&tdo, dout, false, d, N, c.BH) ||
+    if (!make_map(&tq, q, false, d, N, c.BH) || !make_map(&tk, k, false, d, N, B * Hk) ||
+        !make_map(&tv, v, false, d, N, B * Hk) || !make_map(&tdo, dout, false, d, N, c.BH) ||
         !make_map_acc(&tdq, c.dq_acc, d, c.Np, c.BH))
         return ATTN_ERR_CUDA;
     BwdParams bp;
@@ -322,7 +350,9 @@ attn_status attn_bwd_main(const void* q, const void* k, const void* v, const voi
     bp.dv = dv;
     bp.N = N;
     bp.Npad = c.Np;
-    bp.BH = c.BH;
+    bp.BHk = B * Hk;
+    bp.H = H;
+    bp.Hk = Hk;
     bp.n_kv = (N + kTile - 1) / kTile;
     bp.causal = causal;
     bp.cs = scale * 1.44269504088896340736f;
@@ -332,6 +362,16 @@ attn_status attn_bwd_main(const void* q, const void* k, const void* v, const voi
                    cudaSuccess
                ? ATTN_OK
                : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                          void* dv, void* workspace, int B, int H, int N, int d, float scale,
+                          int causal, attn_stream_t stream) {
+    return bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, H, N, d, scale, causal, stream);
 }
 
 attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, int d, float scale,
@@ -368,6 +408,25 @@ attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o,
     if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
     if ((rc = attn_bwd_main(q, k, v, dout, dk, dv, workspace, B, H, N, d, scale, causal, stream)) !=
         ATTN_OK)
+        return rc;
+    return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
+}
+
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, int B, int H, int Hk, int N, int d, float scale, int causal,
+                         attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
+    for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (!aligned16(p)) return ATTN_ERR_INVALID;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_INVALID;
+    if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
+    if ((rc = bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, Hk, N, d, scale, causal,
+                              stream)) != ATTN_OK)
         return rc;
     return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
 }

@@ -185,19 +185,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // those heads' Q, dO and fp32 dQ accumulator stay in L2 while every key
     // tile reduces into them.  Causal: low key tiles (longest loops) of every
     // head first, which keeps the tail of the launch short.
-    const int bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BH)
-                              : static_cast<int>(blockIdx.x / prm.n_kv);
-    const int j = prm.causal ? static_cast<int>(blockIdx.x / prm.BH)
+    const int kv_bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BHk)
+                                 : static_cast<int>(blockIdx.x / prm.n_kv);
+    const int j = prm.causal ? static_cast<int>(blockIdx.x / prm.BHk)
                              : static_cast<int>(blockIdx.x % prm.n_kv);  // key tile
     const int n_q_total = (N + kTile - 1) / kTile;
-    const int n_steps = prm.causal ? n_q_total - j : n_q_total;
+    const int n_qh = prm.causal ? n_q_total - j : n_q_total;  // query tiles per query head
+    // The G query heads sharing this key/value head (G = 1 without grouping) are
+    // visited one after the other; dK and dV accumulate over all of them.
+    const int G = prm.H / prm.Hk;
+    const int q_bh0 = (kv_bh / prm.Hk) * prm.H + (kv_bh % prm.Hk) * G;
+    const int n_steps = G * n_qh;
     // Query tile of step t.  Causal: the diagonal tile j, then upwards.
     // Otherwise each key tile starts at its own index and wraps, so CTAs that
     // run together reduce into different dQ tiles.
     auto q_tile = [&](int t) {
-        const int i = j + t;
+        const int i = j + t % n_qh;
         return (prm.causal || i < n_q_total) ? i : i - n_q_total;
     };
+    auto q_head = [&](int t) { return q_bh0 + t / n_qh; };
 
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
@@ -232,21 +238,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const float* lse2_g = prm.lse2 + static_cast<size_t>(bh) * prm.Npad;
-    const float* dsum_g = prm.dsum + static_cast<size_t>(bh) * prm.Npad;
 
     if (warp == 12) {
         // ================= TMA producer =================
         if (lane == 0) {
             mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
             for (int blk = 0; blk < T::NBLK; ++blk) {
-                tma_load_3d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile, bh);
-                tma_load_3d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile, bh);
+                tma_load_3d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
+                            kv_bh);
+                tma_load_3d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
+                            kv_bh);
             }
             int t = 0;
             for (; t < n_steps; ++t) {
                 const int s = t % T::STAGES;
                 const int i = q_tile(t);
+                const int bh = q_head(t);
                 if (t >= T::STAGES &&
                     !wait_one(b_qdo_empty(s), ((t / T::STAGES) - 1) & 1, abort_flag, prm.st,
                               SITE_QDO_EMPTY))
@@ -259,8 +266,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tma_load_3d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
                                 blk * 64, i * kTile, bh);
                 }
-                bulk_load(sbase + T::OFF_VEC + s * 1024, lse2_g + i * kTile, 512, bf);
-                bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, dsum_g + i * kTile, 512, bf);
+                const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile;
+                bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
+                bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
             }
             wait_drain(b_kv, 0, prm.st, SITE_DRAIN);
             const int first = t > T::STAGES ? t - T::STAGES : 0;
@@ -423,7 +431,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok && wait_warp(b_dkv_full, 0, abort_flag, prm.st, SITE_DKV)) {
             tc_fence_after();
             const bool row_ok = kv_row < N;
-            const size_t roff = (static_cast<size_t>(bh) * N + (row_ok ? kv_row : 0)) * D * 2;
+            const size_t roff = (static_cast<size_t>(kv_bh) * N + (row_ok ? kv_row : 0)) * D * 2;
             const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
             uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
             const float f = h ? prm.scale : 1.f;
@@ -513,7 +521,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
                                                                 : T::OFF_DO + s * T::TILE_BYTES +
                                                                       (u - SLOTS_PER_BUF) * 16384);
-                        tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
+                        tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, q_head(t));
                     }
                     bulk_commit_group();
                 }
@@ -543,7 +551,7 @@ cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, c
     static const cudaError_t attr = cudaFuncSetAttribute(
         bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
-    const long long grid = static_cast<long long>(p.BH) * p.n_kv;
+    const long long grid = static_cast<long long>(p.BHk) * p.n_kv;
     bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq,
                                                                                         p);
     return cudaGetLastError();

@@ -122,6 +122,9 @@ __global__ void __launch_bounds__(320, 1)
         n_t[g] = (qt * kTile >= N) ? 0 : (prm.causal ? min(n_kv_total, qt + 1) : n_kv_total);
     }
     const int n_kv = max(n_t[0], n_t[1]);
+    // Key/value head of this query head (grouped-query attention: H/Hk query
+    // heads share one key/value head; Hk == H is ordinary multi-head attention).
+    const int kv_bh = (bh / prm.H) * prm.Hk + (bh % prm.H) / (prm.H / prm.Hk);
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
@@ -179,7 +182,7 @@ __global__ void __launch_bounds__(320, 1)
                     const CUtensorMap* map = t ? &tm_v : &tm_k;
                     for (int blk = 0; blk < T::NBLK; ++blk)
                         tma_load_3d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
-                                    b_kv_full(slot), blk * T::BLK_ELEMS, j * kTile, bh);
+                                    b_kv_full(slot), blk * T::BLK_ELEMS, j * kTile, kv_bh);
                 }
             }
             // Let every copy this thread started land before the CTA can exit.

@@ -15,7 +15,8 @@ struct FwdParams {
     void* o;          // bf16 [BH, N, D]
     float* lse;       // fp32 [BH, N], natural log of the row normaliser
     int N;            // sequence length (queries = keys)
-    int BH;           // batch * heads
+    int BH;           // batch * query heads
+    int H, Hk;        // query heads, key/value heads (H % Hk == 0; Hk == H without grouping)
     int n_pairs;      // ceil(N / 256): CTAs per head (two 128-row Q tiles each)
     int causal;       // 1: key j visible to query i iff j <= i
     float cs;         // scale * log2(e) (fp8: scale * s_q * s_k * log2(e))
@@ -37,10 +38,12 @@ struct BwdParams {
     const float* lse2;  // workspace (-LSE * log2(e)), see BwdPreParams
     const float* dsum;
     float* dq_acc;
-    void* dk;           // bf16 [BH, N, D]
-    void* dv;           // bf16 [BH, N, D]
-    int N, Npad, BH;
-    int n_kv;           // ceil(N / 128): CTAs per head
+    void* dk;           // bf16 [B*Hk, N, D]
+    void* dv;           // bf16 [B*Hk, N, D]
+    int N, Npad;
+    int BHk;            // batch * key/value heads: CTAs are (kv head, key tile)
+    int H, Hk;          // query heads, key/value heads; each CTA loops over its H/Hk query heads
+    int n_kv;           // ceil(N / 128): CTAs per key/value head
     int causal;
     float cs;           // scale * log2(e)
     float scale;        // softmax scale (applied to dK here and to dQ at conversion)

@@ -123,6 +123,19 @@ def make_inputs(B: int, H: int, N: int, d: int, *, seed: int = 0,
                       seed, rows)
 
 
+def make_inputs_gqa(B: int, H: int, Hk: int, N: int, d: int, *, seed: int = 0,
+                    with_grad: bool = False) -> AttnInputs:
+    """Grouped-query inputs: Q and dO ``[B, H, N, d]``, K and V ``[B, Hk, N, d]``,
+    drawn in the order Q, K, V, dO like ``make_inputs``."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q = _draw(rng, (B, H, N, d))
+    k = _draw(rng, (B, Hk, N, d))
+    v = _draw(rng, (B, Hk, N, d))
+    do = _draw(rng, (B, H, N, d)) if with_grad else None
+    return AttnInputs(B, H, N, d, f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v),
+                      f32_to_bf16_bits(do) if do is not None else None, seed, None)
+
+
 def make_inputs_fp8(B: int, H: int, N: int, d: int, *, seed: int = 0) -> AttnInputsFP8:
     """Draw Q, K, V ~ N(0,1) in float32 and pack each to E4M3 with its own scale."""
     rng = np.random.Generator(np.random.PCG64(seed))

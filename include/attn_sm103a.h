@@ -140,6 +140,26 @@ attn_status attn_bwd_noalloc(const void* q, const void* k, const void* v, const 
                              attn_stream_t stream);
 
 /*
+ * Grouped-query attention (GQA; multi-query attention when Hk = 1): Hk
+ * key/value heads shared by H query heads, H a multiple of Hk; query head h
+ * reads key/value head h / (H / Hk).  q, o: [B, H, N, d]; k, v: [B, Hk, N, d];
+ * lse: [B, H, N].  attn_fwd / attn_bwd are the Hk = H case.
+ * attn_bwd_gqa: dq [B, H, N, d]; dk, dv [B, Hk, N, d], each the sum over the
+ * query heads of its group; workspace = attn_bwd_workspace_bytes(B, H, N, d).
+ * One backward CTA per (batch, key/value head, 128-key tile) visits all query
+ * heads of the group in turn, so dK and dV need no cross-CTA reduction.
+ * Source: FlashAttention-3 walkthrough (runtime parameter num_heads_k; GQA/MQA
+ * listed among its features).  Errors as attn_fwd / attn_bwd, plus
+ * ATTN_ERR_INVALID when Hk < 1 or H % Hk != 0.
+ */
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hk, int N, int d, float scale, int causal, attn_stream_t stream);
+attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
+                         const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                         void* workspace, int B, int H, int Hk, int N, int d, float scale, int causal,
+                         attn_stream_t stream);
+
+/*
  * FP8 forward pass: OCP E4M3 inputs with per-tensor fp32 scales.
  *   q8, k8, v8 : uint8 E4M3 codes [B, H, N, d]; the value read is s * code
  *                (sq, sk, sv finite and > 0).

@@ -4,8 +4,10 @@ Imported by the tests, the smoke check and the benchmark's CPU-baseline leg;
 never by the library.  See ``oracle/attention.py`` for what it computes and
 which passages each function follows.
 """
-from .attention import (backward, bf16_bits_to_f64, causal_visible, e4m3_to_f64,
-                        forward, head_backward, head_forward, scores, softmax_rows)
+from .attention import (backward, backward_gqa, bf16_bits_to_f64, causal_visible, e4m3_to_f64,
+                        forward, forward_gqa, head_backward, head_forward, kv_head_of, scores,
+                        softmax_rows)
 
-__all__ = ["backward", "bf16_bits_to_f64", "causal_visible", "e4m3_to_f64",
-           "forward", "head_backward", "head_forward", "scores", "softmax_rows"]
+__all__ = ["backward", "backward_gqa", "bf16_bits_to_f64", "causal_visible", "e4m3_to_f64",
+           "forward", "forward_gqa", "head_backward", "head_forward", "kv_head_of", "scores",
+           "softmax_rows"]

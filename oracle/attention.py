@@ -19,6 +19,10 @@ What it computes, per (batch, head), materialising S and P in full:
 * a row with no visible key gives ``O_i = 0`` (README example: fully masked
   rows have zero output) and ``LSE_i = +inf`` so that ``exp(S - LSE) = 0``
   there (CUDA softmax item: no -inf - -inf, no divide by zero);
+* grouped-query attention: ``Hk`` key/value heads shared by ``H`` query heads
+  (FlashAttention-3 walkthrough: ``num_heads_k`` runtime parameter, GQA/MQA
+  feature list); query head ``h`` reads key/value head ``h // (H // Hk)``, and
+  the gradient of a shared key/value head is the sum over its query heads;
 * backward of ``O = softmax(scale Q K^T) V`` for a given ``dO``, written from
   the calculus of that definition (the pages cut off before printing it):
   ``dV = P^T dO``, ``dP = dO V^T``, ``D_i = sum_j P_ij dP_ij``,
@@ -185,3 +189,44 @@ def backward(q, k, v, do, scale, causal, heads=None):
         dq, dk, dv, _ = head_backward(q[b, h], k[b, h], v[b, h], do[b, h], scale, causal)
         out[(b, h)] = (dq, dk, dv)
     return out
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query attention
+# ---------------------------------------------------------------------------
+
+
+def kv_head_of(h: int, H: int, Hk: int) -> int:
+    """Key/value head read by query head h."""
+    return h // (H // Hk)
+
+
+def forward_gqa(q, k, v, scale, causal):
+    """Forward with k, v of shape [B, Hk, N, d]: every query head h attends with
+    key/value head kv_head_of(h).  Returns (O [B,H,N,d], LSE [B,H,N])."""
+    B, H = q.shape[0], q.shape[1]
+    Hk = k.shape[1]
+    o = np.zeros(q.shape[:3] + (v.shape[3],), dtype=np.float64)
+    lse = np.zeros(q.shape[:3], dtype=np.float64)
+    for b in range(B):
+        for h in range(H):
+            g = kv_head_of(h, H, Hk)
+            o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, g], v[b, g], scale, causal)
+    return o, lse
+
+
+def backward_gqa(q, k, v, do, scale, causal):
+    """Backward with shared key/value heads: dQ per query head; dK, dV per
+    key/value head, summed over the query heads that read it."""
+    B, H = q.shape[0], q.shape[1]
+    Hk = k.shape[1]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for h in range(H):
+            g = kv_head_of(h, H, Hk)
+            dq[b, h], dkh, dvh, _ = head_backward(q[b, h], k[b, g], v[b, g], do[b, h], scale, causal)
+            dk[b, g] += dkh
+            dv[b, g] += dvh
+    return dq, dk, dv

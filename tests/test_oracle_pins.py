@@ -373,3 +373,64 @@ def test_pins_catch_planted_mistakes(kind):
     o_bf, lse_bf = brute_force_forward(q.tolist(), k.tolist(), v.tolist(), 0.5, causal)
     caught = (not np.allclose(o_m, o_bf, atol=1e-10)) or (not np.allclose(lse_m, lse_bf, atol=1e-10))
     assert caught
+
+
+# ---------------------------------------------------------------------------
+# Grouped-query attention pins
+# ---------------------------------------------------------------------------
+
+
+def test_gqa_with_one_kv_head_per_query_head_is_mha():
+    B, H, N, d = 1, 3, 10, 4
+    q, k, v, do = (rand((B, H, N, d), s) for s in (140, 141, 142, 143))
+    o1, l1 = oracle.forward(q, k, v, 0.5, True)
+    o2, l2 = oracle.forward_gqa(q, k, v, 0.5, True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+    for a, b in zip(oracle.backward(q, k, v, do, 0.5, True), oracle.backward_gqa(q, k, v, do, 0.5, True)):
+        np.testing.assert_allclose(a, b, atol=1e-15)
+
+
+def test_gqa_head_mapping_contiguous_groups():
+    """Query heads 0..G-1 read key/value head 0, heads G..2G-1 read head 1 (the
+    layout of a K projection with Hk heads repeated G times along the head axis)."""
+    assert [oracle.kv_head_of(h, 8, 2) for h in range(8)] == [0, 0, 0, 0, 1, 1, 1, 1]
+    assert [oracle.kv_head_of(h, 6, 1) for h in range(6)] == [0] * 6
+    B, H, Hk, N, d = 1, 4, 2, 7, 3
+    q = rand((B, H, N, d), 150)
+    k, v = rand((B, Hk, N, d), 151), rand((B, Hk, N, d), 152)
+    o, _ = oracle.forward_gqa(q, k, v, 0.9, False)
+    # the same thing written with an explicitly repeated K/V along the head axis
+    o_rep, _ = oracle.forward(q, np.repeat(k, 2, axis=1), np.repeat(v, 2, axis=1), 0.9, False)
+    np.testing.assert_allclose(o, o_rep, atol=1e-15)
+    o_bf, _ = brute_force_forward(q[0, 3].tolist(), k[0, 1].tolist(), v[0, 1].tolist(), 0.9, False)
+    np.testing.assert_allclose(o[0, 3], o_bf, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_backward_matches_finite_differences(causal):
+    B, H, Hk, N, d = 1, 4, 2, 5, 3
+    q = rand((B, H, N, d), 160)
+    k, v = rand((B, Hk, N, d), 161), rand((B, Hk, N, d), 162)
+    do = rand((B, H, N, d), 163)
+    scale = 0.7
+    dq, dk, dv = oracle.backward_gqa(q, k, v, do, scale, causal)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.forward_gqa(qq, kk, vv, scale, causal)
+        return float(np.sum(do * o))
+
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = xp, xm
+            num[idx] = (loss(args_p["q"], args_p["k"], args_p["v"])
+                        - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
+        err = np.linalg.norm(num - g) / np.linalg.norm(num)
+        assert err < 1e-6, (name, err)
