@@ -447,7 +447,21 @@ EXTRA_WORKLOADS = {
     "gqa_b1_h32_hk8_n8192_d128": dict(B=1, H=32, Hk=8, N=8192, d=128, causal=False),
     "gqa_causal_b2_h32_hk4_n4096_d128": dict(B=2, H=32, Hk=4, N=4096, d=128, causal=True),
     "mqa_b4_h16_hk1_n4096_d128": dict(B=4, H=16, Hk=1, N=4096, d=128, causal=False),
+    # sliding window of 1024 keys to the left (and the query itself)
+    "window1024_b1_h32_n8192_d128": dict(B=1, H=32, Hk=32, N=8192, d=128, causal=False,
+                                         window=(1024, 0)),
+    # few heads, long sequence: forward with key tiles split across CTAs
+    "splitkv_b1_h2_n16384_d128": dict(B=1, H=2, Hk=2, N=16384, d=128, causal=False, splitkv=True),
 }
+
+
+def window_flops(N, d, left, right):
+    """Multiply-add work of the visible (query, key) pairs, 4*d per pair."""
+    import numpy as np
+    i = np.arange(N)
+    lo = np.zeros(N) if left < 0 else np.maximum(0, i - left)
+    hi = np.full(N, N - 1) if right < 0 else np.minimum(N - 1, i + right)
+    return 4.0 * d * float(np.sum(hi - lo + 1))
 
 
 def run_extra(args):
@@ -474,13 +488,28 @@ def run_extra(args):
     ws = torch.empty(api.bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
 
+    window = w.get("window")
+    if w.get("splitkv"):
+        ws_split = torch.empty(api.load_library().attn_fwd_splitkv_workspace_bytes(B, H, N, D, 0),
+                               dtype=torch.uint8, device="cuda")
+
     def step(ev=None):
         if ev:
             ev[0].record(stream)
-        api.fwd(q, k, v, causal=causal, o=o, lse=lse)
+        if window is not None:
+            api.fwd_window(q, k, v, *window, o=o, lse=lse)
+        elif w.get("splitkv"):
+            api.fwd_splitkv(q, k, v, num_splits=0, causal=causal, o=o, lse=lse, workspace=ws_split)
+        else:
+            api.fwd(q, k, v, causal=causal, o=o, lse=lse)
         if ev:
             ev[1].record(stream)
-        api.bwd(q, k, v, o, do, lse, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
+        if window is not None:
+            api.bwd_window(q, k, v, o, do, lse, *window, dq=dq, dk=dk, dv=dv, workspace=ws)
+        elif w.get("splitkv"):
+            api.fwd(q, k, v, causal=causal, o=o, lse=lse)  # single-pass forward, for comparison
+        else:
+            api.bwd(q, k, v, o, do, lse, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
         if ev:
             ev[2].record(stream)
 
@@ -498,8 +527,20 @@ def run_extra(args):
     fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
     bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
     f = attn_flops(B, H, N, D, causal)
+    if window is not None:
+        f = B * H * window_flops(N, D, *window)
     peaks, kind = load_peaks()
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if w.get("splitkv"):
+        line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
+                "unit": "TFLOP/s", "value": round(f / (fwd_ms * 1e-3) / 1e12, 2),
+                "components": {
+                    "fwd_splitkv": {"ms": round(fwd_ms, 4), "tflops": round(f / (fwd_ms * 1e-3) / 1e12, 1)},
+                    "fwd_single_pass": {"ms": round(bwd_ms, 4),
+                                        "tflops": round(f / (bwd_ms * 1e-3) / 1e12, 1)}},
+                "dtype": "bf16", "data": "synthetic"}
+        print(json.dumps(line), flush=True)
+        return 0
     line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
             "value": round(3.5 * f / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
             "components": {

@@ -34,6 +34,11 @@ SIGNATURES = {
     "attn_fwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_bwd_gqa": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f,
                           _i, _vp]),
+    "attn_fwd_splitkv_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "attn_fwd_splitkv": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "attn_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
+    "attn_bwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
+                             _f, _i, _i, _vp]),
     "attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_check_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
@@ -118,6 +123,75 @@ def fwd(q, k, v, scale: float | None = None, causal: bool = False, o=None, lse=N
                                                 o.data_ptr(), lse.data_ptr(), B, H, Hk, N, d, scale,
                                                 int(bool(causal)), _stream_handle(stream)))
     return o, lse
+
+
+def fwd_splitkv(q, k, v, num_splits: int = 0, scale: float | None = None, causal: bool = False,
+                o=None, lse=None, workspace=None, stream=None):
+    """Split-KV forward (bf16, Hk = H): returns (O, LSE) like ``fwd``."""
+    import torch
+    B, H, N, d = q.shape
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _check_qkv(name, t, (B, H, N, d), torch.bfloat16)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    lib = load_library()
+    need = int(lib.attn_fwd_splitkv_workspace_bytes(B, H, N, d, int(num_splits)))
+    if need == 0:
+        raise ValueError("invalid sizes or num_splits")
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("attn_fwd_splitkv", lib.attn_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                                    o.data_ptr(), lse.data_ptr(),
+                                                    workspace.data_ptr(), B, H, N, d, scale,
+                                                    int(bool(causal)), int(num_splits),
+                                                    _stream_handle(stream)))
+    return o, lse
+
+
+def fwd_window(q, k, v, window_left: int, window_right: int, scale: float | None = None,
+               o=None, lse=None, stream=None):
+    """Sliding-window forward: key j visible to query i iff
+    i - window_left <= j <= i + window_right (-1: unbounded side)."""
+    import torch
+    B, H, N, d = q.shape
+    Hk = k.shape[1]
+    _check_qkv("q", q, (B, H, N, d), torch.bfloat16)
+    for name, t in (("k", k), ("v", v)):
+        _check_qkv(name, t, (B, Hk, N, d), torch.bfloat16)
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("attn_fwd_window", load_library().attn_fwd_window(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), lse.data_ptr(), B, H, Hk, N, d,
+        scale, int(window_left), int(window_right), _stream_handle(stream)))
+    return o, lse
+
+
+def bwd_window(q, k, v, o, dout, lse, window_left: int, window_right: int,
+               scale: float | None = None, dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Sliding-window backward; dK, dV have K's head count."""
+    import torch
+    B, H, N, d = q.shape
+    Hk = k.shape[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for name, t in (("q", q), ("o", o), ("dout", dout), ("dq", dq)):
+        _check_qkv(name, t, (B, H, N, d), torch.bfloat16)
+    for name, t in (("k", k), ("v", v), ("dk", dk), ("dv", dv)):
+        _check_qkv(name, t, (B, Hk, N, d), torch.bfloat16)
+    need = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check("attn_bwd_window", load_library().attn_bwd_window(
+        q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(), dout.data_ptr(), lse.data_ptr(),
+        dq.data_ptr(), dk.data_ptr(), dv.data_ptr(), workspace.data_ptr(), B, H, Hk, N, d, scale,
+        int(window_left), int(window_right), _stream_handle(stream)))
+    return dq, dk, dv
 
 
 def bwd_workspace_bytes(B: int, H: int, N: int, d: int) -> int:

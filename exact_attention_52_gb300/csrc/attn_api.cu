@@ -189,7 +189,12 @@ extern "C" {
 namespace {
 
 attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                       int Hk, int N, int d, float scale, int causal, attn_stream_t stream) {
+                       int Hk, int N, int d, float scale, int causal, attn_stream_t stream,
+                       int win_left = -2, int win_right = -2) {
+    if (win_left == -2) {  // no explicit window: the causal flag decides
+        win_left = -1;
+        win_right = causal ? 0 : -1;
+    }
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
     if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
@@ -211,12 +216,35 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
     p.Hk = Hk;
     p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
     p.causal = causal;
+    p.win_left = win_left;
+    p.win_right = win_right;
     p.cs = scale * 1.44269504088896340736f;
     p.out_scale = 1.f;
+    p.n_splits = 1;
+    p.split_len = (N + kTile - 1) / kTile;
+    p.o_part = nullptr;
+    p.lse_part = nullptr;
     p.st = dev_status(ds);
     return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
                : ATTN_ERR_CUDA;
+}
+
+// Number of key-tile splits: the smallest that gives about two waves of CTAs
+// on the SMs, at most one split per key tile and at most kMaxSplits.
+constexpr int kMaxSplits = 16;
+int auto_splits(int BH, int N, int num_sms) {
+    const long long ctas = static_cast<long long>(BH) * ((N + 2 * kTile - 1) / (2 * kTile));
+    const int n_kv = (N + kTile - 1) / kTile;
+    int s = 1;
+    while (s < kMaxSplits && s < n_kv && ctas * s < 2ll * num_sms) s *= 2;
+    return s < n_kv ? s : n_kv;
+}
+
+size_t splitkv_bytes(int B, int H, int N, int d, int S) {
+    const size_t rows = static_cast<size_t>(B) * H * N;
+    return round256(static_cast<size_t>(S) * rows * d * sizeof(float)) +
+           round256(static_cast<size_t>(S) * rows * sizeof(float));
 }
 
 }  // namespace
@@ -231,6 +259,77 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
                          int H, int Hk, int N, int d, float scale, int causal, attn_stream_t stream) {
     return fwd_common(q, k, v, o, lse, B, H, Hk, N, d, scale, causal, stream);
+}
+
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
+    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+    if (num_splits == 0) num_splits = kMaxSplits;  // enough for any automatic choice
+    return splitkv_bytes(B, H, N, d, num_splits);
+}
+
+attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             void* workspace, int B, int H, int N, int d, float scale, int causal,
+                             int num_splits, attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_INVALID;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_INVALID;
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+    const int BH = B * H;
+    const int n_kv = (N + kTile - 1) / kTile;
+    int S = num_splits;
+    if (S == 0) {
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        S = auto_splits(BH, N, sms);
+    }
+    if (S > n_kv) S = n_kv;
+    const int split_len = (n_kv + S - 1) / S;
+    S = (n_kv + split_len - 1) / split_len;  // no empty trailing split
+    if (S <= 1) return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
+
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, BH) ||
+        !make_map(&tv, v, false, d, N, BH))
+        return ATTN_ERR_CUDA;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    const size_t rows = static_cast<size_t>(BH) * N;
+    FwdParams p;
+    p.o = o;
+    p.lse = lse;
+    p.N = N;
+    p.BH = BH;
+    p.H = H;
+    p.Hk = H;
+    p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
+    p.causal = causal;
+    p.win_left = -1;
+    p.win_right = causal ? 0 : -1;
+    p.cs = scale * 1.44269504088896340736f;
+    p.out_scale = 1.f;
+    p.n_splits = S;
+    p.split_len = split_len;
+    p.o_part = reinterpret_cast<float*>(ws);
+    p.lse_part = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(S) * rows * d * sizeof(float)));
+    p.st = dev_status(ds);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_fwd_bf16(d, tq, tk, tv, p, st) != cudaSuccess) return ATTN_ERR_CUDA;
+    CombineParams c;
+    c.o_part = p.o_part;
+    c.lse_part = p.lse_part;
+    c.o = o;
+    c.lse = lse;
+    c.S = S;
+    c.BH = BH;
+    c.N = N;
+    c.D = d;
+    return launch_splitkv_combine(c, st) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float sq, float sk, float sv,
@@ -259,8 +358,14 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
     p.Hk = H;
     p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
     p.causal = causal;
+    p.win_left = -1;
+    p.win_right = causal ? 0 : -1;
     p.cs = scale * sq * sk * 1.44269504088896340736f;
     p.out_scale = sv;
+    p.n_splits = 1;
+    p.split_len = (N + kTile - 1) / kTile;
+    p.o_part = nullptr;
+    p.lse_part = nullptr;
     p.st = dev_status(ds);
     return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
@@ -330,7 +435,12 @@ namespace {
 
 attn_status bwd_main_common(const void* q, const void* k, const void* v, const void* dout, void* dk,
                             void* dv, void* workspace, int B, int H, int Hk, int N, int d, float scale,
-                            int causal, attn_stream_t stream) {
+                            int causal, attn_stream_t stream, int win_left = -2,
+                            int win_right = -2) {
+    if (win_left == -2) {
+        win_left = -1;
+        win_right = causal ? 0 : -1;
+    }
     for (const void* p : {q, k, v, dout, static_cast<const void*>(dk), static_cast<const void*>(dv)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
     if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
@@ -355,6 +465,8 @@ attn_status bwd_main_common(const void* q, const void* k, const void* v, const v
     bp.Hk = Hk;
     bp.n_kv = (N + kTile - 1) / kTile;
     bp.causal = causal;
+    bp.win_left = win_left;
+    bp.win_right = win_right;
     bp.cs = scale * 1.44269504088896340736f;
     bp.scale = scale;
     bp.st = dev_status(c.ds);
@@ -427,6 +539,36 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
     if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
     if ((rc = bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, Hk, N, d, scale, causal,
                               stream)) != ATTN_OK)
+        return rc;
+    return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
+}
+
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                            int H, int Hk, int N, int d, float scale, int window_left,
+                            int window_right, attn_stream_t stream) {
+    if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID;
+    const int causal = (window_left == -1 && window_right == 0) ? 1 : 0;
+    return fwd_common(q, k, v, o, lse, B, H, Hk, N, d, scale, causal, stream, window_left,
+                      window_right);
+}
+
+attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, int B, int H, int Hk, int N, int d, float scale,
+                            int window_left, int window_right, attn_stream_t stream) {
+    if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID;
+    const int causal = (window_left == -1 && window_right == 0) ? 1 : 0;
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
+    for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
+                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
+        if (!aligned16(p)) return ATTN_ERR_INVALID;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_INVALID;
+    if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
+    if ((rc = bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, Hk, N, d, scale, causal, stream,
+                              window_left, window_right)) != ATTN_OK)
         return rc;
     return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
 }

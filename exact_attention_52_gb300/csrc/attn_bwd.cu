@@ -190,18 +190,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const int j = prm.causal ? static_cast<int>(blockIdx.x / prm.BHk)
                              : static_cast<int>(blockIdx.x % prm.n_kv);  // key tile
     const int n_q_total = (N + kTile - 1) / kTile;
-    const int n_qh = prm.causal ? n_q_total - j : n_q_total;  // query tiles per query head
+    // Query tiles [q_lo, q_lo + n_qh) hold the rows that see some key of this
+    // tile (window i - win_left <= key <= i + win_right; negative = no bound).
+    const int kr0 = j * kTile, kr1 = min(N - 1, j * kTile + kTile - 1);
+    const int qrow_lo = prm.win_right < 0 ? 0 : max(0, kr0 - prm.win_right);
+    const int qrow_hi = prm.win_left < 0 ? N - 1 : min(N - 1, kr1 + prm.win_left);
+    const int q_lo = qrow_lo / kTile;
+    const int n_qh = qrow_lo <= qrow_hi ? qrow_hi / kTile - q_lo + 1 : 0;  // per query head
+    const bool full_range = (q_lo == 0 && n_qh == n_q_total);
     // The G query heads sharing this key/value head (G = 1 without grouping) are
     // visited one after the other; dK and dV accumulate over all of them.
     const int G = prm.H / prm.Hk;
     const int q_bh0 = (kv_bh / prm.Hk) * prm.H + (kv_bh % prm.Hk) * G;
     const int n_steps = G * n_qh;
-    // Query tile of step t.  Causal: the diagonal tile j, then upwards.
-    // Otherwise each key tile starts at its own index and wraps, so CTAs that
-    // run together reduce into different dQ tiles.
+    // Query tile of step t.  Over the full range each key tile starts at its
+    // own index and wraps, so CTAs that run together reduce into different dQ
+    // tiles; otherwise (causal, windows) the range is walked upwards, which
+    // already starts neighbouring key tiles on different query tiles.
     auto q_tile = [&](int t) {
+        if (!full_range) return q_lo + t % n_qh;
         const int i = j + t % n_qh;
-        return (prm.causal || i < n_q_total) ? i : i - n_q_total;
+        return i < n_q_total ? i : i - n_q_total;
     };
     auto q_head = [&](int t) { return q_bh0 + t / n_qh; };
 
@@ -380,8 +389,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 break;
             }
             tc_fence_after();
-            // diagonal tile: query column h*64 + c visible iff h*64 + c >= r
-            const int cmin = (prm.causal && i == j) ? r - h * 64 : 0;
+            // query column c of this half (row qc0 + c) sees key kv_row iff
+            // cmin <= c <= cmax
+            const int qc0 = i * kTile + h * 64;
+            const int cmin = prm.win_right < 0 ? -kTile : kv_row - prm.win_right - qc0;
+            const int cmax = prm.win_left < 0 ? 2 * kTile : kv_row + prm.win_left - qc0;
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {  // two chunks of 32 query columns
                 const int c0 = cc * 32;
@@ -405,8 +417,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float x0, x1, t0, t1, d0, d1;
                         ffma2(x0, x1, u2f(sv[e + h2]), u2f(sv[e + h2 + 1]), cs, cs, nlv[h2], nlv[h2 + 1]);
                         float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        if (c < cmin) p0 = 0.f;
-                        if (c + 1 < cmin) p1 = 0.f;
+                        if (c < cmin || c > cmax) p0 = 0.f;
+                        if (c + 1 < cmin || c + 1 > cmax) p1 = 0.f;
                         pk[(e + h2) / 2] = pack_bf16x2(p0, p1);
                         fsub2(t0, t1, u2f(dp[e + h2]), u2f(dp[e + h2 + 1]), ddv[h2], ddv[h2 + 1]);
                         fmul2(d0, d1, p0, p1, t0, t1);

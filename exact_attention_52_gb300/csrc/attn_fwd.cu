@@ -104,24 +104,42 @@ __global__ void __launch_bounds__(320, 1)
     }
 
     // ---- work assignment ----
-    // Non-causal: head-major order, so the CTAs resident at any time cover
-    // only a few heads and each head's K and V come from HBM about once.
-    // Causal: heaviest query tiles of every head first (longest-first keeps
-    // the tail of the launch short; a causal head needs half the K/V reuse).
-    const int bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BH)
-                              : static_cast<int>(blockIdx.x / prm.n_pairs);
+    // Without a mask (and for sliding windows) head-major order, so the CTAs
+    // resident at any time cover only a few heads and each head's K and V come
+    // from HBM about once.  Causal: heaviest query tiles of every head first
+    // (longest-first keeps the tail of the launch short).
+    // Split-KV: the splits of one query-tile pair are adjacent CTAs.
+    const unsigned cta = blockIdx.x / prm.n_splits;
+    const int split = static_cast<int>(blockIdx.x % prm.n_splits);
+    const bool split_mode = prm.n_splits > 1;
+    const bool lpt = prm.causal != 0;
+    const int bh = lpt ? static_cast<int>(cta % prm.BH) : static_cast<int>(cta / prm.n_pairs);
     const int pair = prm.n_pairs - 1 -
-                     (prm.causal ? static_cast<int>(blockIdx.x / prm.BH)
-                                 : static_cast<int>(blockIdx.x % prm.n_pairs));
+                     (lpt ? static_cast<int>(cta / prm.BH) : static_cast<int>(cta % prm.n_pairs));
     const int N = prm.N;
     const int n_kv_total = (N + kTile - 1) / kTile;
-    int n_t[2];
+    // Query tile g of this CTA uses key tiles [lo_t[g], lo_t[g] + n_t[g]): the
+    // tiles holding keys visible to some row of the tile (window
+    // i - win_left <= key <= i + win_right, a negative bound meaning none),
+    // cut to this CTA's split.
+    int lo_t[2], n_t[2];
 #pragma unroll
     for (int g = 0; g < 2; ++g) {
         const int qt = 2 * pair + g;
-        n_t[g] = (qt * kTile >= N) ? 0 : (prm.causal ? min(n_kv_total, qt + 1) : n_kv_total);
+        const int r0 = qt * kTile, r1 = min(N - 1, qt * kTile + kTile - 1);
+        const int key_lo = prm.win_left < 0 ? 0 : max(0, r0 - prm.win_left);
+        const int key_hi = prm.win_right < 0 ? N - 1 : min(N - 1, r1 + prm.win_right);
+        const int lo = max(key_lo / kTile, split * prm.split_len);
+        const int hi = min(key_hi / kTile, split * prm.split_len + prm.split_len - 1);
+        const bool live = r0 < N && key_lo <= key_hi && hi >= lo;
+        lo_t[g] = live ? lo : 0;
+        n_t[g] = live ? hi - lo + 1 : 0;
     }
-    const int n_kv = max(n_t[0], n_t[1]);
+    // The CTA streams key tiles [kv_lo, kv_lo + n_kv): the union of both ranges
+    // (they overlap or touch: the two tiles' rows are adjacent).
+    const int kv_lo = n_t[0] > 0 ? (n_t[1] > 0 ? min(lo_t[0], lo_t[1]) : lo_t[0]) : lo_t[1];
+    const int kv_hi = max(n_t[0] > 0 ? lo_t[0] + n_t[0] : 0, n_t[1] > 0 ? lo_t[1] + n_t[1] : 0);
+    const int n_kv = (n_t[0] > 0 || n_t[1] > 0) ? kv_hi - kv_lo : 0;
     // Key/value head of this query head (grouped-query attention: H/Hk query
     // heads share one key/value head; Hk == H is ordinary multi-head attention).
     const int kv_bh = (bh / prm.H) * prm.Hk + (bh % prm.H) / (prm.H / prm.Hk);
@@ -182,7 +200,7 @@ __global__ void __launch_bounds__(320, 1)
                     const CUtensorMap* map = t ? &tm_v : &tm_k;
                     for (int blk = 0; blk < T::NBLK; ++blk)
                         tma_load_3d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
-                                    b_kv_full(slot), blk * T::BLK_ELEMS, j * kTile, kv_bh);
+                                    b_kv_full(slot), blk * T::BLK_ELEMS, (kv_lo + j) * kTile, kv_bh);
                 }
             }
             // Let every copy this thread started land before the CTA can exit.
@@ -206,7 +224,7 @@ __global__ void __launch_bounds__(320, 1)
             // S_g = Q_g K_j^T : both operands K-major, 32 bytes of K per instruction.
             auto issue_s = [&](int g, int j) {
                 const uint32_t qa = sq_base + g * T::TILE_BYTES;
-                const uint32_t kb = slot_addr(2 * j);
+                const uint32_t kb = slot_addr(2 * (j - kv_lo));
 #pragma unroll
                 for (int kk = 0; kk < D / T::UMMA_K; ++kk) {
                     const uint32_t off = (kk * 32) / 128 * T::BLK_BYTES + (kk * 32) % 128;
@@ -216,58 +234,84 @@ __global__ void __launch_bounds__(320, 1)
                 mma_commit(b_s_full + 8u * g);
             };
             // O_g += P_g V_j : P from tensor memory, V MN-major (rows = keys).
-            auto issue_pv = [&](int g, int j) {
-                const uint32_t vb = slot_addr(2 * j + 1);
+            auto issue_pv = [&](int g, int j, bool first) {
+                const uint32_t vb = slot_addr(2 * (j - kv_lo) + 1);
 #pragma unroll
                 for (int kk = 0; kk < kTile / T::UMMA_K; ++kk) {
                     mma_ts<FP8>(tmem + (g ? T::COL_O1 : T::COL_O0),
                                 tmem + (g ? T::COL_S1 : T::COL_S0) + kk * 8,
                                 sw128_desc(vb + kk * T::UMMA_K * 128, T::BLK_BYTES, 1024), T::IDESC_PV,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+                                (!first || kk > 0) ? 1u : 0u);
                 }
             };
+            // Ring index of K_j / V_j (j absolute), in the producer's load order.
+            auto kidx = [&](int j) { return 2 * (j - kv_lo); };
+            auto active = [&](int g, int j) { return n_t[g] > 0 && j >= lo_t[g] && j < lo_t[g] + n_t[g]; };
             auto run = [&]() -> bool {
                 if (!wait_one(b_q, 0, abort_flag, prm.st, SITE_Q)) return false;
-                if (!wait_kv(0)) return false;
+                if (n_kv == 0) return true;
+                if (!wait_kv(kidx(kv_lo))) return false;
                 tc_fence_after();
-                if (n_t[0] > 0) issue_s(0, 0);
-                if (n_t[1] > 0) issue_s(1, 0);
-                mma_commit(b_kv_empty(0));
-                for (int j = 0; j < n_kv; ++j) {
+                if (active(0, kv_lo)) issue_s(0, kv_lo);
+                if (active(1, kv_lo)) issue_s(1, kv_lo);
+                mma_commit(b_kv_empty(kidx(kv_lo) % T::KV_SLOTS));
+                for (int j = kv_lo; j < kv_lo + n_kv; ++j) {
+                    const bool has_next = j + 1 < kv_lo + n_kv;
                     bool v_ready = false, k_next_ready = false;
-                    if (j < n_t[0]) {
-                        if (!wait_one(b_p_full, j & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
-                        if (!wait_kv(2 * j + 1)) return false;
+                    auto need_k_next = [&]() -> bool {
+                        if (k_next_ready) return true;
+                        if (!wait_kv(kidx(j + 1))) return false;
+                        k_next_ready = true;
+                        return true;
+                    };
+                    // query tile 0: PV_0(j), then S_0(j+1)
+                    if (active(0, j)) {
+                        if (!wait_one(b_p_full, (j - lo_t[0]) & 1, abort_flag, prm.st, SITE_P_FULL))
+                            return false;
+                        if (!wait_kv(kidx(j) + 1)) return false;
                         v_ready = true;
                         tc_fence_after();
-                        issue_pv(0, j);
-                        if (j + 1 < n_t[0]) {
-                            if (!wait_kv(2 * j + 2)) return false;
-                            k_next_ready = true;
+                        issue_pv(0, j, j == lo_t[0]);
+                        if (active(0, j + 1)) {
+                            if (!need_k_next()) return false;
                             tc_fence_after();
                             issue_s(0, j + 1);
                         } else {
                             mma_commit(b_o_full);
                         }
-                    }
-                    if (j < n_t[1]) {
-                        if (!wait_one(b_p_full + 8u, j & 1, abort_flag, prm.st, SITE_P_FULL))
-                            return false;
-                        if (!v_ready && !wait_kv(2 * j + 1)) return false;
+                    } else if (active(0, j + 1)) {
+                        if (!need_k_next()) return false;
                         tc_fence_after();
-                        issue_pv(1, j);
+                        issue_s(0, j + 1);
                     }
-                    mma_commit(b_kv_empty((2 * j + 1) % T::KV_SLOTS));  // V_j consumed
-                    if (j < n_t[1]) {
-                        if (j + 1 < n_t[1]) {
-                            if (!k_next_ready && !wait_kv(2 * j + 2)) return false;
+                    // query tile 1: PV_1(j), release V_j, then S_1(j+1)
+                    if (active(1, j)) {
+                        if (!wait_one(b_p_full + 8u, (j - lo_t[1]) & 1, abort_flag, prm.st, SITE_P_FULL))
+                            return false;
+                        if (!v_ready && !wait_kv(kidx(j) + 1)) return false;
+                        v_ready = true;
+                        tc_fence_after();
+                        issue_pv(1, j, j == lo_t[1]);
+                    }
+                    if (!v_ready && !wait_kv(kidx(j) + 1)) return false;  // loaded, never used
+                    mma_commit(b_kv_empty((kidx(j) + 1) % T::KV_SLOTS));  // V_j consumed
+                    if (active(1, j)) {
+                        if (active(1, j + 1)) {
+                            if (!need_k_next()) return false;
                             tc_fence_after();
                             issue_s(1, j + 1);
                         } else {
                             mma_commit(b_o_full + 8u);
                         }
+                    } else if (active(1, j + 1)) {
+                        if (!need_k_next()) return false;
+                        tc_fence_after();
+                        issue_s(1, j + 1);
                     }
-                    if (j + 1 < n_kv) mma_commit(b_kv_empty((2 * j + 2) % T::KV_SLOTS));  // K_{j+1}
+                    if (has_next) {
+                        if (!need_k_next()) return false;
+                        mma_commit(b_kv_empty(kidx(j + 1) % T::KV_SLOTS));  // K_{j+1} consumed
+                    }
                 }
                 return true;
             };
@@ -283,12 +327,15 @@ __global__ void __launch_bounds__(320, 1)
         const int row = wq * 32 + lane;  // row within the tile
         const int q_row = (2 * pair + g) * kTile + row;
         const int n = g ? n_t[1] : n_t[0];
+        const int jt0 = g ? lo_t[1] : lo_t[0];  // first key tile of this query tile
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + (g ? T::COL_S1 : T::COL_S0) + lane_off;
         const uint32_t tO = tmem + (g ? T::COL_O1 : T::COL_O0) + lane_off;
         const uint32_t b_sf = b_s_full + 8u * g, b_pf = b_p_full + 8u * g, b_of = b_o_full + 8u * g;
         const float cs = prm.cs;
-        const int row_limit = prm.causal ? min(N, q_row + 1) : N;  // keys [0, row_limit) visible
+        // keys [key_min, key_max] are visible to this row
+        const int key_min = prm.win_left < 0 ? 0 : q_row - prm.win_left;
+        const int key_max = prm.win_right < 0 ? N - 1 : min(N - 1, q_row + prm.win_right);
 
         float m_used = -INFINITY;  // running max in log2 units of the scaled scores
         float l_sum = 0.f;         // running sum of 2^(s*cs - m_used), unrounded (for LSE)
@@ -306,13 +353,14 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
 
-            const int lim = row_limit - j * kTile;  // columns >= lim are masked
-            if (lim < kTile) {
+            const int kv0 = (jt0 + j) * kTile;
+            const int c_lo = key_min - kv0, c_hi = key_max - kv0;  // visible columns [c_lo, c_hi]
+            if (c_lo > 0 || c_hi < kTile - 1) {
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; ++i)
-                        if (c * 32 + i >= lim) s[c][i] = f2u(-INFINITY);
+                        if (c * 32 + i < c_lo || c * 32 + i > c_hi) s[c][i] = f2u(-INFINITY);
             }
             float mx8[8];
 #pragma unroll
@@ -410,7 +458,40 @@ __global__ void __launch_bounds__(320, 1)
             if (lane == 0) mbar_arrive(b_pf);
         }
 
-        if (ok && n > 0 && wait_warp(b_of, 0, abort_flag, prm.st, SITE_O_FULL)) {
+        if (split_mode && ok && n == 0 && q_row < N) {
+            // this split holds no key visible to the tile: an empty partial
+            float4* op = reinterpret_cast<float4*>(
+                prm.o_part + ((static_cast<size_t>(split) * prm.BH + bh) * N + q_row) * D);
+#pragma unroll
+            for (int c = 0; c < D / 4; ++c) op[c] = make_float4(0.f, 0.f, 0.f, 0.f);
+            prm.lse_part[(static_cast<size_t>(split) * prm.BH + bh) * N + q_row] = -INFINITY;
+        }
+        const bool o_ready = ok && n > 0 && wait_warp(b_of, 0, abort_flag, prm.st, SITE_O_FULL);
+        if (o_ready && split_mode) {
+            // fp32 partial for the combine kernel: O over this split's keys, and its LSE
+            tc_fence_after();
+            const bool row_ok = q_row < N;
+            const float l_norm = FP8 ? l_sum : l_pv;
+            const float inv_l = l_norm > 0.f ? prm.out_scale / l_norm : 0.f;
+            float* op = prm.o_part + ((static_cast<size_t>(split) * prm.BH + bh) * N +
+                                      (row_ok ? q_row : 0)) * D;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tO + 32 * c, o);
+                tmem_ld_wait(o);
+                if (row_ok) {
+#pragma unroll
+                    for (int v = 0; v < 8; ++v)
+                        reinterpret_cast<float4*>(op + c * 32)[v] =
+                            make_float4(u2f(o[4 * v]) * inv_l, u2f(o[4 * v + 1]) * inv_l,
+                                        u2f(o[4 * v + 2]) * inv_l, u2f(o[4 * v + 3]) * inv_l);
+                }
+            }
+            if (row_ok)
+                prm.lse_part[(static_cast<size_t>(split) * prm.BH + bh) * N + q_row] =
+                    l_sum > 0.f ? (m_used + log2f(l_sum)) * kLn2 : -INFINITY;
+        } else if (o_ready) {
             tc_fence_after();
             const bool row_ok = q_row < N;
             const float l_norm = FP8 ? l_sum : l_pv;
@@ -448,6 +529,43 @@ __global__ void __launch_bounds__(320, 1)
     }
 }
 
+// Merge of split-KV partials, one warp per (head, row): with m = max_s LSE_s
+// and w_s = exp(LSE_s - m), O = sum_s w_s O_s / sum_s w_s and
+// LSE = m + ln(sum_s w_s) -- the running-max / running-sum combination of the
+// FlashAttention digest (section 2) applied to whole partial results.
+__global__ void __launch_bounds__(256) splitkv_combine_kernel(const CombineParams p) {
+    const int lane = threadIdx.x & 31;
+    const long long rows = static_cast<long long>(p.BH) * p.N;
+    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+    const int epl = p.D / 32;  // elements per lane: 2 or 4
+    for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
+        float m = -INFINITY;
+        for (int sp = 0; sp < p.S; ++sp) m = fmaxf(m, p.lse_part[sp * rows + r]);
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+        float wsum = 0.f;
+        if (m != -INFINITY) {
+            for (int sp = 0; sp < p.S; ++sp) {
+                const float w = expf(p.lse_part[sp * rows + r] - m);
+                wsum += w;
+                const float* src = p.o_part + (sp * rows + r) * p.D + lane * epl;
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (e < epl) acc[e] += w * src[e];
+            }
+        }
+        const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
+        uint16_t* dst = static_cast<uint16_t*>(p.o) + r * p.D + lane * epl;
+        if (epl == 4) {
+            const uint32_t w0 = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            const uint32_t w1 = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+            *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);
+        } else {
+            *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        }
+        if (lane == 0) p.lse[r] = wsum > 0.f ? m + logf(wsum) : INFINITY;
+    }
+}
+
 template <int D, bool FP8>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream) {
@@ -455,7 +573,7 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     static const cudaError_t attr = cudaFuncSetAttribute(
         fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
-    const long long grid = static_cast<long long>(p.BH) * p.n_pairs;
+    const long long grid = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
     fwd_kernel<D, FP8><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
@@ -473,6 +591,14 @@ cudaError_t launch_fwd_fp8(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream) {
     if (D == 128) return launch_fwd_impl<128, true>(tq, tk, tv, p, stream);
     return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_splitkv_combine(const CombineParams& p, cudaStream_t stream) {
+    const long long rows = static_cast<long long>(p.BH) * p.N;
+    const long long blocks = (rows + 7) / 8;
+    const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
+    splitkv_combine_kernel<<<grid, 256, 0, stream>>>(p);
+    return cudaGetLastError();
 }
 
 int fwd_smem_bytes(int D, bool fp8) {

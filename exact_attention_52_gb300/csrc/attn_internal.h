@@ -18,10 +18,27 @@ struct FwdParams {
     int BH;           // batch * query heads
     int H, Hk;        // query heads, key/value heads (H % Hk == 0; Hk == H without grouping)
     int n_pairs;      // ceil(N / 256): CTAs per head (two 128-row Q tiles each)
-    int causal;       // 1: key j visible to query i iff j <= i
+    int causal;       // 1: causal mask (also selects longest-first launch order)
+    int win_left;     // key j visible to query i iff i - win_left <= j <= i + win_right;
+    int win_right;    // a negative bound is no bound (causal: -1, 0; full: -1, -1)
     float cs;         // scale * log2(e) (fp8: scale * s_q * s_k * log2(e))
     float out_scale;  // 1 (bf16) or s_v (fp8)
+    // Split-KV mode (n_splits > 1): CTA s of a query-tile pair covers key tiles
+    // [s * split_len, (s + 1) * split_len) and writes an fp32 partial result
+    // (O normalised over its keys, and its log-sum-exp) instead of o and lse.
+    int n_splits;
+    int split_len;
+    float* o_part;    // fp32 [n_splits, BH, N, D]
+    float* lse_part;  // fp32 [n_splits, BH, N]; -inf where a split saw no key
     DevStatus st;
+};
+
+struct CombineParams {
+    const float* o_part;    // fp32 [S, BH, N, D]
+    const float* lse_part;  // fp32 [S, BH, N]
+    void* o;                // bf16 [BH, N, D]
+    float* lse;             // fp32 [BH, N]
+    int S, BH, N, D;
 };
 
 struct BwdPreParams {
@@ -44,7 +61,9 @@ struct BwdParams {
     int BHk;            // batch * key/value heads: CTAs are (kv head, key tile)
     int H, Hk;          // query heads, key/value heads; each CTA loops over its H/Hk query heads
     int n_kv;           // ceil(N / 128): CTAs per key/value head
-    int causal;
+    int causal;         // causal mask (also selects longest-first launch order)
+    int win_left;       // window bounds as in FwdParams (negative: none)
+    int win_right;
     float cs;           // scale * log2(e)
     float scale;        // softmax scale (applied to dK here and to dQ at conversion)
     DevStatus st;
@@ -63,6 +82,7 @@ cudaError_t launch_fwd_bf16(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_fwd_fp8(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream);
+cudaError_t launch_splitkv_combine(const CombineParams& p, cudaStream_t stream);
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdq,
                             const BwdParams& p, cudaStream_t stream);

@@ -160,6 +160,43 @@ attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void
                          attn_stream_t stream);
 
 /*
+ * Split-KV forward for problems too small to fill the GPU (few heads, long
+ * sequences): the key tiles of every query-tile pair are divided among
+ * `num_splits` CTAs, each writing an fp32 partial (O over its keys and that
+ * log-sum-exp) to `workspace`; a combine kernel then merges the partials with
+ * the running-max / running-sum rule and writes o (bf16) and lse as attn_fwd.
+ *   num_splits : 1..16, or 0 to choose (about two waves of CTAs); 1 is attn_fwd.
+ *   workspace  : attn_fwd_splitkv_workspace_bytes(B, H, N, d, num_splits) bytes,
+ *                256-byte aligned, caller-owned (num_splits = 0: room for 16).
+ * Two launches on `stream`.  Source: ai.engineer item 59 (small-query work
+ * split across thread blocks plus a separate combining kernel); FlashAttention-3
+ * tuning page (num_splits runtime parameter); the merge is the online-softmax
+ * combination of the FlashAttention digest, section 2.
+ */
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits);
+attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             void* workspace, int B, int H, int N, int d, float scale, int causal,
+                             int num_splits, attn_stream_t stream);
+
+/*
+ * Sliding-window (local) attention, with grouped heads as in attn_fwd_gqa:
+ * key j is visible to query i iff i - window_left <= j <= i + window_right;
+ * -1 removes that bound (window_left = -1, window_right = 0 is causal;
+ * -1, -1 is no mask).  Key tiles outside every row's window are skipped in
+ * both passes.  Arguments otherwise as attn_fwd_gqa / attn_bwd_gqa; bounds
+ * below -1 give ATTN_ERR_INVALID.
+ * Source: FlashAttention-3 tuning page (Is_local, window_size_left /
+ * window_size_right runtime parameters).
+ */
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                            int H, int Hk, int N, int d, float scale, int window_left,
+                            int window_right, attn_stream_t stream);
+attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o,
+                            const void* dout, const float* lse, void* dq, void* dk, void* dv,
+                            void* workspace, int B, int H, int Hk, int N, int d, float scale,
+                            int window_left, int window_right, attn_stream_t stream);
+
+/*
  * FP8 forward pass: OCP E4M3 inputs with per-tensor fp32 scales.
  *   q8, k8, v8 : uint8 E4M3 codes [B, H, N, d]; the value read is s * code
  *                (sq, sk, sv finite and > 0).

@@ -19,6 +19,9 @@ What it computes, per (batch, head), materialising S and P in full:
 * a row with no visible key gives ``O_i = 0`` (README example: fully masked
   rows have zero output) and ``LSE_i = +inf`` so that ``exp(S - LSE) = 0``
   there (CUDA softmax item: no -inf - -inf, no divide by zero);
+* sliding-window (local) attention: key j visible to query i iff
+  i - left <= j <= i + right, a negative bound meaning none (FlashAttention-3
+  tuning page, window sizes); (-1, 0) is the causal mask;
 * grouped-query attention: ``Hk`` key/value heads shared by ``H`` query heads
   (FlashAttention-3 walkthrough: ``num_heads_k`` runtime parameter, GQA/MQA
   feature list); query head ``h`` reads key/value head ``h // (H // Hk)``, and
@@ -90,12 +93,33 @@ def causal_visible(nq: int, nk: int, rows: np.ndarray | None = None) -> np.ndarr
     return j[None, :] <= (i[:, None] + (nk - nq))
 
 
+def window_visible(nq: int, nk: int, window: tuple[int, int],
+                   rows: np.ndarray | None = None) -> np.ndarray:
+    """Boolean [len(rows), nk] mask of a local (sliding-window) attention:
+    key j is visible to query i iff i' - left <= j <= i' + right, where
+    i' = i + (nk - nq) aligns the last query with the last key (as the causal
+    rule does) and a negative bound is no bound (FlashAttention-3 tuning page:
+    window_size_left / window_size_right)."""
+    left, right = window
+    i = (np.arange(nq) if rows is None else np.asarray(rows)) + (nk - nq)
+    j = np.arange(nk)
+    vis = np.ones((len(i), nk), dtype=bool)
+    if right >= 0:
+        vis &= j[None, :] <= i[:, None] + right
+    if left >= 0:
+        vis &= j[None, :] >= i[:, None] - left
+    return vis
+
+
 def scores(q: np.ndarray, k: np.ndarray, scale: float, causal: bool,
-           rows: np.ndarray | None = None) -> np.ndarray:
-    """S = scale * Q K^T for one head ([Nq, d] x [Nk, d]); masked entries are -inf."""
+           rows: np.ndarray | None = None, window: tuple[int, int] | None = None) -> np.ndarray:
+    """S = scale * Q K^T for one head ([Nq, d] x [Nk, d]); masked entries are -inf.
+    ``window`` (left, right), when given, replaces the causal flag."""
     qq = q if rows is None else q[rows]
     s = float(scale) * (qq @ k.T)
-    if causal:
+    if window is not None:
+        s = np.where(window_visible(q.shape[0], k.shape[0], window, rows), s, -np.inf)
+    elif causal:
         s = np.where(causal_visible(q.shape[0], k.shape[0], rows), s, -np.inf)
     return s
 
@@ -116,9 +140,9 @@ def softmax_rows(s: np.ndarray) -> tuple[np.ndarray, np.ndarray]:
     return p, lse
 
 
-def head_forward(q, k, v, scale, causal, rows=None):
+def head_forward(q, k, v, scale, causal, rows=None, window=None):
     """One head: returns (O [rows, d], LSE [rows], P [rows, Nk])."""
-    p, lse = softmax_rows(scores(q, k, scale, causal, rows))
+    p, lse = softmax_rows(scores(q, k, scale, causal, rows, window))
     return p @ v, lse, p
 
 
@@ -153,12 +177,12 @@ def forward(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float,
 # ---------------------------------------------------------------------------
 
 
-def head_backward(q, k, v, do, scale, causal):
+def head_backward(q, k, v, do, scale, causal, window=None):
     """One head: gradients of O = softmax(scale Q K^T) V for upstream dO.
 
     Returns (dQ, dK, dV, D) with D_i = sum_j P_ij dP_ij.
     """
-    o, _, p = head_forward(q, k, v, scale, causal)
+    o, _, p = head_forward(q, k, v, scale, causal, window=window)
     dv = p.T @ do
     dp = do @ v.T
     dsum = np.sum(p * dp, axis=1)
@@ -201,7 +225,7 @@ def kv_head_of(h: int, H: int, Hk: int) -> int:
     return h // (H // Hk)
 
 
-def forward_gqa(q, k, v, scale, causal):
+def forward_gqa(q, k, v, scale, causal, window=None):
     """Forward with k, v of shape [B, Hk, N, d]: every query head h attends with
     key/value head kv_head_of(h).  Returns (O [B,H,N,d], LSE [B,H,N])."""
     B, H = q.shape[0], q.shape[1]
@@ -211,11 +235,12 @@ def forward_gqa(q, k, v, scale, causal):
     for b in range(B):
         for h in range(H):
             g = kv_head_of(h, H, Hk)
-            o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, g], v[b, g], scale, causal)
+            o[b, h], lse[b, h], _ = head_forward(q[b, h], k[b, g], v[b, g], scale, causal,
+                                                 window=window)
     return o, lse
 
 
-def backward_gqa(q, k, v, do, scale, causal):
+def backward_gqa(q, k, v, do, scale, causal, window=None):
     """Backward with shared key/value heads: dQ per query head; dK, dV per
     key/value head, summed over the query heads that read it."""
     B, H = q.shape[0], q.shape[1]
@@ -226,7 +251,8 @@ def backward_gqa(q, k, v, do, scale, causal):
     for b in range(B):
         for h in range(H):
             g = kv_head_of(h, H, Hk)
-            dq[b, h], dkh, dvh, _ = head_backward(q[b, h], k[b, g], v[b, g], do[b, h], scale, causal)
+            dq[b, h], dkh, dvh, _ = head_backward(q[b, h], k[b, g], v[b, g], do[b, h], scale, causal,
+                                                  window=window)
             dk[b, g] += dkh
             dv[b, g] += dvh
     return dq, dk, dv

@@ -56,6 +56,17 @@ def test_workspace_bytes(lib):
     assert lib.attn_bwd_workspace_bytes(1, 1, 1, 96) == 0
 
 
+def test_splitkv_workspace_bytes(lib):
+    B, H, N, d = 1, 2, 1000, 128
+    rows = B * H * N
+    r256 = lambda x: (x + 255) // 256 * 256
+    for S in (1, 3, 16):
+        assert lib.attn_fwd_splitkv_workspace_bytes(B, H, N, d, S) == r256(S * rows * d * 4) + r256(S * rows * 4)
+    assert lib.attn_fwd_splitkv_workspace_bytes(B, H, N, d, 0) == lib.attn_fwd_splitkv_workspace_bytes(B, H, N, d, 16)
+    assert lib.attn_fwd_splitkv_workspace_bytes(B, H, N, d, 17) == 0
+    assert lib.attn_fwd_splitkv_workspace_bytes(B, H, N, 96, 2) == 0
+
+
 def test_smem_budget(lib):
     for which, d in ((0, 64), (0, 128), (1, 128), (2, 64), (2, 128)):
         b = lib.attn_kernel_smem_bytes(which, d)

@@ -434,3 +434,81 @@ def test_gqa_backward_matches_finite_differences(causal):
                         - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
         err = np.linalg.norm(num - g) / np.linalg.norm(num)
         assert err < 1e-6, (name, err)
+
+
+# ---------------------------------------------------------------------------
+# Sliding-window pins
+# ---------------------------------------------------------------------------
+
+
+def test_window_special_cases_are_causal_and_full():
+    np.testing.assert_array_equal(A.window_visible(9, 9, (-1, 0)), A.causal_visible(9, 9))
+    assert A.window_visible(9, 9, (-1, -1)).all()
+    np.testing.assert_array_equal(A.window_visible(5, 2, (-1, 0)), A.causal_visible(5, 2))
+    # window (1, 2) on 6 rows: row i sees i-1 .. i+2
+    expect = np.array([[abs(j - i) <= 2 and j >= i - 1 for j in range(6)] for i in range(6)])
+    np.testing.assert_array_equal(A.window_visible(6, 6, (1, 2)), expect)
+
+
+def test_window_zero_returns_own_value_row():
+    N, d = 11, 4
+    q, k, v = rand((N, d), 170), rand((N, d), 171), rand((N, d), 172)
+    o, lse, _ = A.head_forward(q, k, v, 0.6, False, window=(0, 0))
+    np.testing.assert_allclose(o, v, atol=1e-15)
+    np.testing.assert_allclose(lse, 0.6 * np.sum(q * k, axis=1), atol=1e-14)
+
+
+def test_window_one_left_is_a_sigmoid_of_two_keys():
+    N, d = 7, 4
+    q, k, v = rand((N, d), 173), rand((N, d), 174), rand((N, d), 175)
+    o, _, _ = A.head_forward(q, k, v, 0.5, False, window=(1, 0))
+    for i in range(1, N):
+        s0, s1 = 0.5 * q[i] @ k[i - 1], 0.5 * q[i] @ k[i]
+        w0 = 1.0 / (1.0 + math.exp(s1 - s0))
+        np.testing.assert_allclose(o[i], w0 * v[i - 1] + (1 - w0) * v[i], atol=1e-14)
+
+
+def brute_force_window(q, k, v, scale, left, right):
+    n = len(q)
+    o = []
+    for i in range(n):
+        vis = [j for j in range(n) if (right < 0 or j <= i + right) and (left < 0 or j >= i - left)]
+        s = {j: scale * math.fsum(a * b for a, b in zip(q[i], k[j])) for j in vis}
+        m = max(s.values())
+        e = {j: math.exp(s[j] - m) for j in vis}
+        z = math.fsum(e.values())
+        o.append([math.fsum(e[j] * v[j][c] for j in vis) / z for c in range(len(v[0]))])
+    return np.array(o)
+
+
+@pytest.mark.parametrize("window", [(2, 1), (0, 3), (4, -1), (-1, 2)])
+def test_window_brute_force(window):
+    N, d = 12, 5
+    q, k, v = rand((N, d), 180), rand((N, d), 181), rand((N, d), 182)
+    o, _, _ = A.head_forward(q, k, v, 0.4, False, window=window)
+    np.testing.assert_allclose(o, brute_force_window(q.tolist(), k.tolist(), v.tolist(), 0.4, *window),
+                               atol=1e-13)
+
+
+@pytest.mark.parametrize("window", [(2, 1), (1, 0)])
+def test_window_backward_matches_finite_differences(window):
+    N, d = 6, 3
+    q, k, v, do = (rand((N, d), s) for s in (190, 191, 192, 193))
+    dq, dk, dv, _ = A.head_backward(q, k, v, do, 0.8, False, window=window)
+
+    def loss(qq, kk, vv):
+        o, _, _ = A.head_forward(qq, kk, vv, 0.8, False, window=window)
+        return float(np.sum(do * o))
+
+    h = 1e-6
+    for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        num = np.zeros_like(x)
+        for idx in np.ndindex(*x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += h
+            xm[idx] -= h
+            a = {"q": q, "k": k, "v": v}
+            b = dict(a)
+            a[name], b[name] = xp, xm
+            num[idx] = (loss(a["q"], a["k"], a["v"]) - loss(b["q"], b["k"], b["v"])) / (2 * h)
+        assert np.linalg.norm(num - g) / np.linalg.norm(num) < 1e-6, name
