@@ -450,8 +450,8 @@ EXTRA_WORKLOADS = {
     # sliding window of 1024 keys to the left (and the query itself)
     "window1024_b1_h32_n8192_d128": dict(B=1, H=32, Hk=32, N=8192, d=128, causal=False,
                                          window=(1024, 0)),
-    # few heads, long sequence: forward with key tiles split across CTAs
-    "splitkv_b1_h2_n16384_d128": dict(B=1, H=2, Hk=2, N=16384, d=128, causal=False, splitkv=True),
+    # one head, long sequence (64 CTAs without splitting): key tiles split across CTAs
+    "splitkv_b1_h1_n16384_d128": dict(B=1, H=1, Hk=1, N=16384, d=128, causal=False, splitkv=True),
 }
 
 

@@ -230,14 +230,16 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
                : ATTN_ERR_CUDA;
 }
 
-// Number of key-tile splits: the smallest that gives about two waves of CTAs
-// on the SMs, at most one split per key tile and at most kMaxSplits.
+// Number of key-tile splits: none while the CTAs already cover most SMs
+// (the partials and the combine then cost more than they give back), else
+// the smallest power of two that covers them, at most one split per key tile
+// and at most kMaxSplits.
 constexpr int kMaxSplits = 16;
 int auto_splits(int BH, int N, int num_sms) {
     const long long ctas = static_cast<long long>(BH) * ((N + 2 * kTile - 1) / (2 * kTile));
     const int n_kv = (N + kTile - 1) / kTile;
     int s = 1;
-    while (s < kMaxSplits && s < n_kv && ctas * s < 2ll * num_sms) s *= 2;
+    while (s < kMaxSplits && s < n_kv && ctas * s * 4 < 3ll * num_sms) s *= 2;
     return s < n_kv ? s : n_kv;
 }
 
