@@ -31,6 +31,8 @@
 // MN-major, as the A operand dS of dQ.
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include "attn_internal.h"
 #include "ptx.cuh"
 
@@ -390,12 +392,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             tc_fence_after();
             // query column c of this half (row qc0 + c) sees key kv_row iff
-            // cmin <= c <= cmax
+            // cmin <= c <= cmax; the mask is applied only where some row of the
+            // warp needs it (boundary tiles of a causal mask or a window)
             const int qc0 = i * kTile + h * 64;
             const int cmin = prm.win_right < 0 ? -kTile : kv_row - prm.win_right - qc0;
             const int cmax = prm.win_left < 0 ? 2 * kTile : kv_row + prm.win_left - qc0;
-#pragma unroll
-            for (int cc = 0; cc < 2; ++cc) {  // two chunks of 32 query columns
+            const bool masked = __any_sync(0xffffffffu, cmin > 0 || cmax < 63);
+            auto chunk = [&](auto masked_tag, int cc) {
+                constexpr bool kMasked = decltype(masked_tag)::value;
                 const int c0 = cc * 32;
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tS + c0, sv);
@@ -417,8 +421,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         float x0, x1, t0, t1, d0, d1;
                         ffma2(x0, x1, u2f(sv[e + h2]), u2f(sv[e + h2 + 1]), cs, cs, nlv[h2], nlv[h2 + 1]);
                         float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        if (c < cmin || c > cmax) p0 = 0.f;
-                        if (c + 1 < cmin || c + 1 > cmax) p1 = 0.f;
+                        if constexpr (kMasked) {
+                            if (c < cmin || c > cmax) p0 = 0.f;
+                            if (c + 1 < cmin || c + 1 > cmax) p1 = 0.f;
+                        }
                         pk[(e + h2) / 2] = pack_bf16x2(p0, p1);
                         fsub2(t0, t1, u2f(dp[e + h2]), u2f(dp[e + h2 + 1]), ddv[h2], ddv[h2 + 1]);
                         fmul2(d0, d1, p0, p1, t0, t1);
@@ -432,6 +438,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int v = 0; v < 4; ++v)
                     *reinterpret_cast<uint4*>(ds_row + (((cc * 4 + v) ^ sw) << 4)) =
                         make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3]);
+            };
+            if (masked) {
+                chunk(std::true_type{}, 0);
+                chunk(std::true_type{}, 1);
+            } else {
+                chunk(std::false_type{}, 0);
+                chunk(std::false_type{}, 1);
             }
             tmem_st_wait();
             fence_proxy_async_smem();

@@ -247,9 +247,57 @@ __global__ void __launch_bounds__(320, 1)
             // Ring index of K_j / V_j (j absolute), in the producer's load order.
             auto kidx = [&](int j) { return 2 * (j - kv_lo); };
             auto active = [&](int g, int j) { return n_t[g] > 0 && j >= lo_t[g] && j < lo_t[g] + n_t[g]; };
+            // Both query tiles start at kv_lo (no mask, causal, split): the tiles
+            // differ only in where they stop, and the loop runs on relative indices.
+            auto run_aligned = [&]() -> bool {
+                if (!wait_kv(0)) return false;
+                tc_fence_after();
+                if (n_t[0] > 0) issue_s(0, kv_lo);
+                if (n_t[1] > 0) issue_s(1, kv_lo);
+                mma_commit(b_kv_empty(0));
+                for (int j = 0; j < n_kv; ++j) {
+                    bool v_ready = false, k_next_ready = false;
+                    if (j < n_t[0]) {
+                        if (!wait_one(b_p_full, j & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                        if (!wait_kv(2 * j + 1)) return false;
+                        v_ready = true;
+                        tc_fence_after();
+                        issue_pv(0, kv_lo + j, j == 0);
+                        if (j + 1 < n_t[0]) {
+                            if (!wait_kv(2 * j + 2)) return false;
+                            k_next_ready = true;
+                            tc_fence_after();
+                            issue_s(0, kv_lo + j + 1);
+                        } else {
+                            mma_commit(b_o_full);
+                        }
+                    }
+                    if (j < n_t[1]) {
+                        if (!wait_one(b_p_full + 8u, j & 1, abort_flag, prm.st, SITE_P_FULL))
+                            return false;
+                        if (!v_ready && !wait_kv(2 * j + 1)) return false;
+                        tc_fence_after();
+                        issue_pv(1, kv_lo + j, j == 0);
+                    }
+                    mma_commit(b_kv_empty((2 * j + 1) % T::KV_SLOTS));  // V_j consumed
+                    if (j < n_t[1]) {
+                        if (j + 1 < n_t[1]) {
+                            if (!k_next_ready && !wait_kv(2 * j + 2)) return false;
+                            tc_fence_after();
+                            issue_s(1, kv_lo + j + 1);
+                        } else {
+                            mma_commit(b_o_full + 8u);
+                        }
+                    }
+                    if (j + 1 < n_kv) mma_commit(b_kv_empty((2 * j + 2) % T::KV_SLOTS));  // K_{j+1}
+                }
+                return true;
+            };
             auto run = [&]() -> bool {
                 if (!wait_one(b_q, 0, abort_flag, prm.st, SITE_Q)) return false;
                 if (n_kv == 0) return true;
+                if ((n_t[0] == 0 || lo_t[0] == kv_lo) && (n_t[1] == 0 || lo_t[1] == kv_lo))
+                    return run_aligned();
                 if (!wait_kv(kidx(kv_lo))) return false;
                 tc_fence_after();
                 if (active(0, kv_lo)) issue_s(0, kv_lo);
