@@ -209,12 +209,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // own index and wraps, so CTAs that run together reduce into different dQ
     // tiles; otherwise (causal, windows) the range is walked upwards, which
     // already starts neighbouring key tiles on different query tiles.
-    auto q_tile = [&](int t) {
-        if (!full_range) return q_lo + t % n_qh;
-        const int i = j + t % n_qh;
+    auto q_tile = [&](int tt) {  // tt: step index within one query head
+        if (!full_range) return q_lo + tt;
+        const int i = j + tt;
         return i < n_q_total ? i : i - n_q_total;
     };
-    auto q_head = [&](int t) { return q_bh0 + t / n_qh; };
 
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
@@ -261,10 +260,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             kv_bh);
             }
             int t = 0;
-            for (; t < n_steps; ++t) {
+            int tt = 0, bh = q_bh0;  // step t = (head bh - q_bh0) * n_qh + tt
+            for (; t < n_steps; ++t, ++tt) {
+                if (tt == n_qh) {
+                    tt = 0;
+                    ++bh;
+                }
                 const int s = t % T::STAGES;
-                const int i = q_tile(t);
-                const int bh = q_head(t);
+                const int i = q_tile(tt);
                 if (t >= T::STAGES &&
                     !wait_one(b_qdo_empty(s), ((t / T::STAGES) - 1) & 1, abort_flag, prm.st,
                               SITE_QDO_EMPTY))
@@ -377,9 +380,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int sw = r & 7;
         const uint32_t b_sf = b_s_full + 8u * h, b_pf = b_p_full + 8u * h;
         bool ok = true;
-        for (int t = 0; t < n_steps; ++t) {
+        for (int t = 0, tt = 0; t < n_steps; ++t, ++tt) {
+            if (tt == n_qh) tt = 0;
             const int s = t % T::STAGES;
-            const int i = q_tile(t);
+            const int i = q_tile(tt);
             const float* nlse2 =
                 reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024) + h * 64;
             const float* dsum = nlse2 + 128;
@@ -489,9 +493,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const bool leader = (warp == 8 && lane == 0);
         constexpr int SLOTS_PER_BUF = T::TILE_BYTES / (kTile * 128);  // 16 KB boxes per buffer
         bool ok = true;
-        for (int t = 0; t < n_steps && ok; ++t) {
+        int tt = 0, bh = q_bh0;
+        for (int t = 0; t < n_steps && ok; ++t, ++tt) {
+            if (tt == n_qh) {
+                tt = 0;
+                ++bh;
+            }
             const int s = t % T::STAGES;
-            const int i = q_tile(t);
+            const int i = q_tile(tt);
 #pragma unroll
             for (int p = 0; p < T::NDQ; ++p) {
                 if (!wait_warp(b_dq_full + 8u * p, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
@@ -546,7 +555,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                              (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
                                                                 : T::OFF_DO + s * T::TILE_BYTES +
                                                                       (u - SLOTS_PER_BUF) * 16384);
-                        tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, q_head(t));
+                        tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
                     }
                     bulk_commit_group();
                 }
