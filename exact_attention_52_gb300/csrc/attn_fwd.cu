@@ -441,14 +441,15 @@ __global__ void __launch_bounds__(320, 1)
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
-                        const float p0 = ex2_approx(fmaf(u2f(s[c][i + 0]), cs, -m_sub));
-                        const float p1 = ex2_approx(fmaf(u2f(s[c][i + 1]), cs, -m_sub));
-                        const float p2 = ex2_approx(fmaf(u2f(s[c][i + 2]), cs, -m_sub));
-                        const float p3 = ex2_approx(fmaf(u2f(s[c][i + 3]), cs, -m_sub));
-                        ls[0] += p0;
-                        ls[1] += p1;
-                        ls[2] += p2;
-                        ls[3] += p3;
+                        float x0, x1, x2, x3;
+                        ffma2(x0, x1, u2f(s[c][i]), u2f(s[c][i + 1]), cs, cs, -m_sub, -m_sub);
+                        ffma2(x2, x3, u2f(s[c][i + 2]), u2f(s[c][i + 3]), cs, cs, -m_sub, -m_sub);
+                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                        float a0, a1;
+                        fadd2(a0, a1, p0, p1, p2, p3);
+                        fadd2(ls[(i >> 2) & 1], ls[2 + ((i >> 2) & 1)], ls[(i >> 2) & 1],
+                              ls[2 + ((i >> 2) & 1)], a0, a1);
                         pk[c * 8 + i / 4] = pack_e4m3x4(p0, p1, p2, p3);
                     }
                 tmem_st32(tS, pk);
