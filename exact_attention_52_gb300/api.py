@@ -20,8 +20,16 @@ ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID", -2: "ATTN_ERR_UNSUPPORTED",
                 -3: "ATTN_ERR_CUDA", -4: "ATTN_ERR_TIMEOUT"}
 
+
+
+class Strides(ctypes.Structure):
+    """attn_strides_t: element strides (b, h, n) of a [B, heads, N, d] view."""
+    _fields_ = [("b", ctypes.c_int64), ("h", ctypes.c_int64), ("n", ctypes.c_int64)]
+
+
 # Every symbol the header declares, with (restype, argtypes).
 _vp, _i, _f, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_st = Strides
 SIGNATURES = {
     "attn_fwd": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_bwd_workspace_bytes": (_sz, [_i, _i, _i, _i]),
@@ -39,6 +47,10 @@ SIGNATURES = {
     "attn_fwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "attn_bwd_window": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i,
                              _f, _i, _i, _vp]),
+    "attn_fwd_strided": (_i, [_vp, _st, _vp, _st, _vp, _st, _vp, _st, _vp, _i, _i, _i, _i, _i, _f,
+                              _i, _i, _vp]),
+    "attn_bwd_strided": (_i, [_vp, _st, _vp, _st, _vp, _st, _vp, _st, _vp, _st, _vp, _vp, _st, _vp,
+                              _st, _vp, _st, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp]),
     "attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_check_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
@@ -299,4 +311,69 @@ def bwd_stages(q, k, v, o, dout, lse, dq, dk, dv, workspace, scale: float, causa
                                                           B, H, N, d, float(scale), h))
     if ev[3] is not None:
         ev[3].record(stream)
+    return dq, dk, dv
+
+
+def _bhnd_strides(t, layout):
+    """Strides of a 4-D CUDA tensor seen as [B, heads, N, d]: layout "bhnd" (the
+    tensor is [B, heads, N, d]) or "bnhd" (the tensor is [B, N, heads, d])."""
+    sb, s1, s2, sd = t.stride()
+    if sd != 1:
+        raise ValueError("the last (d) dimension must be contiguous")
+    if layout == "bhnd":
+        return Strides(sb, s1, s2)
+    if layout == "bnhd":
+        return Strides(sb, s2, s1)
+    raise ValueError(f"unknown layout {layout!r}")
+
+
+def _bhnd_shape(t, layout):
+    B, a, b, d = t.shape
+    return (B, a, b, d) if layout == "bhnd" else (B, b, a, d)
+
+
+def fwd_strided(q, k, v, layout: str = "bnhd", scale: float | None = None, window=(-1, -1),
+                o=None, lse=None, stream=None):
+    """Forward on bf16 tensors of any strides with a contiguous last dimension.
+    ``layout`` says how the 4 dimensions are ordered ("bnhd": [B, N, H, d] as
+    produced by most projections; "bhnd": [B, H, N, d]).  Returns (O in the same
+    layout as q, LSE [B, H, N])."""
+    import torch
+    B, H, N, d = _bhnd_shape(q, layout)
+    Hk = _bhnd_shape(k, layout)[1]
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or t.dtype != torch.bfloat16:
+            raise ValueError(f"{name} must be a bf16 CUDA tensor")
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    o = torch.empty_like(q) if o is None else o
+    if lse is None:
+        lse = torch.empty((B, H, N), dtype=torch.float32, device=q.device)
+    _check("attn_fwd_strided", load_library().attn_fwd_strided(
+        q.data_ptr(), _bhnd_strides(q, layout), k.data_ptr(), _bhnd_strides(k, layout),
+        v.data_ptr(), _bhnd_strides(v, layout), o.data_ptr(), _bhnd_strides(o, layout),
+        lse.data_ptr(), B, H, Hk, N, d, scale, int(window[0]), int(window[1]),
+        _stream_handle(stream)))
+    return o, lse
+
+
+def bwd_strided(q, k, v, o, dout, lse, layout: str = "bnhd", scale: float | None = None,
+                window=(-1, -1), dq=None, dk=None, dv=None, workspace=None, stream=None):
+    """Backward counterpart of ``fwd_strided``; gradients take the layout of
+    their inputs (dq like q, dk like k, dv like v)."""
+    import torch
+    B, H, N, d = _bhnd_shape(q, layout)
+    Hk = _bhnd_shape(k, layout)[1]
+    scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = bwd_workspace_bytes(B, H, N, d)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    st = lambda t: _bhnd_strides(t, layout)
+    _check("attn_bwd_strided", load_library().attn_bwd_strided(
+        q.data_ptr(), st(q), k.data_ptr(), st(k), v.data_ptr(), st(v), o.data_ptr(), st(o),
+        dout.data_ptr(), st(dout), lse.data_ptr(), dq.data_ptr(), st(dq), dk.data_ptr(), st(dk),
+        dv.data_ptr(), st(dv), workspace.data_ptr(), B, H, Hk, N, d, scale, int(window[0]),
+        int(window[1]), _stream_handle(stream)))
     return dq, dk, dv

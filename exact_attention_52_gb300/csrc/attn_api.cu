@@ -83,18 +83,21 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
-// 3-D view {d, N, B*H} of a dense [B, H, N, d] tensor; box {inner, 128, 1},
-// 128-byte swizzle, out-of-range rows read as zero.
-bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int BH) {
+// 4-D view {d, N, heads, B} of a [B, heads, N, d] tensor with element strides
+// s (d contiguous); box {128 bytes of d, 128 rows, 1, 1}, 128-byte swizzle,
+// rows >= N read as zero.
+bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int heads, int B,
+              const Strides& st) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t eb = fp8 ? 1 : 2;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
-                                static_cast<cuuint64_t>(BH)};
-    const cuuint64_t strides[2] = {d * eb, static_cast<cuuint64_t>(N) * d * eb};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / eb), 128u, 1u};
-    const cuuint32_t estr[3] = {1u, 1u, 1u};
-    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N),
+                                static_cast<cuuint64_t>(heads), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(st.n) * eb, static_cast<cuuint64_t>(st.h) * eb,
+                                   static_cast<cuuint64_t>(st.b) * eb};
+    const cuuint32_t box[4] = {static_cast<cuuint32_t>(128 / eb), 128u, 1u, 1u};
+    const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+    return enc(m, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
@@ -118,6 +121,23 @@ bool make_map_acc(CUtensorMap* m, const float* base, int d, int Npad, int BH) {
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+Strides dense(int heads, int N, int d) {
+    Strides s;
+    s.n = d;
+    s.h = static_cast<long long>(N) * d;
+    s.b = static_cast<long long>(heads) * N * d;
+    return s;
+}
+
+// Strides usable by TMA and by the 16-byte vector stores: non-negative,
+// multiples of 16 bytes, below 2^40 bytes.
+bool strides_ok(const Strides& s, int elem_bytes) {
+    for (long long x : {s.b, s.h, s.n}) {
+        if (x < 0 || (x * elem_bytes) % 16 != 0 || x * elem_bytes >= (1ll << 40)) return false;
+    }
+    return true;
+}
+
 constexpr long long kMaxElems = (1ll << 40);  // keeps every byte offset well inside 64 bits
 
 attn_status check_sizes(int B, int H, int N, int d, float scale, int causal) {
@@ -131,9 +151,15 @@ attn_status check_sizes(int B, int H, int N, int d, float scale, int causal) {
     if (bh * N * d > kMaxElems) return ATTN_ERR_INVALID;
     const long long ctas = bh * ((N + 2 * kTile - 1) / (2 * kTile));
     const long long ctas_bwd = bh * ((N + kTile - 1) / kTile);
-    if (ctas > 0x7fffffffll || ctas_bwd > 0x7fffffffll) return ATTN_ERR_INVALID;
+    if (ctas > 0x7fffffffll / 16 || ctas_bwd > 0x7fffffffll) return ATTN_ERR_INVALID;
     return ATTN_OK;
 }
+
+attn_status check_group(int H, int Hk) {
+    return (Hk >= 1 && Hk <= H && H % Hk == 0) ? ATTN_OK : ATTN_ERR_INVALID;
+}
+
+attn_status check_window(int wl, int wr) { return (wl >= -1 && wr >= -1) ? ATTN_OK : ATTN_ERR_INVALID; }
 
 long long npad(int N) { return (static_cast<long long>(N) + kTile - 1) / kTile * kTile; }
 
@@ -171,47 +197,43 @@ __global__ void wait_selftest_kernel(DevStatus st) {
     __syncthreads();
 }
 
-}  // namespace
+// ---------------------------------------------------------------------------
+// Launch paths shared by the entry points (all arguments validated here)
+// ---------------------------------------------------------------------------
 
-cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream) {
-    wait_selftest_kernel<<<1, 64, 0, stream>>>(st);
-    return cudaGetLastError();
-}
+// Split-KV partial buffers (null: single pass).
+struct SplitArgs {
+    int n_splits = 1;
+    int split_len = 0;
+    float* o_part = nullptr;
+    float* lse_part = nullptr;
+};
 
-}  // namespace attn
-
-using namespace attn;
-
-extern "C" {
-
-}  // extern "C"
-
-namespace {
-
-attn_status fwd_common(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                       int Hk, int N, int d, float scale, int causal, attn_stream_t stream,
-                       int win_left = -2, int win_right = -2) {
-    if (win_left == -2) {  // no explicit window: the causal flag decides
-        win_left = -1;
-        win_right = causal ? 0 : -1;
-    }
+attn_status fwd_run(const void* q, const Strides& qs, const void* k, const Strides& ks, const void* v,
+                    const Strides& vs, void* o, const Strides& os, float* lse, int B, int H, int Hk,
+                    int N, int d, float scale, int win_left, int win_right, attn_stream_t stream,
+                    const SplitArgs& split = SplitArgs()) {
+    const int causal = (win_left == -1 && win_right == 0) ? 1 : 0;
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
-    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
+    if ((rc = check_group(H, Hk)) != ATTN_OK || (rc = check_window(win_left, win_right)) != ATTN_OK)
+        return rc;
     if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_INVALID;
+    if (!strides_ok(qs, 2) || !strides_ok(ks, 2) || !strides_ok(vs, 2) || !strides_ok(os, 2))
         return ATTN_ERR_INVALID;
     DeviceState* ds = nullptr;
     if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-    const int BH = B * H;
     CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, B * Hk) ||
-        !make_map(&tv, v, false, d, N, B * Hk))
+    if (!make_map(&tq, q, false, d, N, H, B, qs) || !make_map(&tk, k, false, d, N, Hk, B, ks) ||
+        !make_map(&tv, v, false, d, N, Hk, B, vs))
         return ATTN_ERR_CUDA;
     FwdParams p;
     p.o = o;
+    p.os = os;
     p.lse = lse;
     p.N = N;
-    p.BH = BH;
+    p.BH = B * H;
     p.H = H;
     p.Hk = Hk;
     p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
@@ -220,10 +242,10 @@ attn_status fwd_common(const void* q, const void* k, const void* v, void* o, flo
     p.win_right = win_right;
     p.cs = scale * 1.44269504088896340736f;
     p.out_scale = 1.f;
-    p.n_splits = 1;
-    p.split_len = (N + kTile - 1) / kTile;
-    p.o_part = nullptr;
-    p.lse_part = nullptr;
+    p.n_splits = split.n_splits;
+    p.split_len = split.n_splits > 1 ? split.split_len : (N + kTile - 1) / kTile;
+    p.o_part = split.o_part;
+    p.lse_part = split.lse_part;
     p.st = dev_status(ds);
     return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
@@ -248,138 +270,6 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S) {
     return round256(static_cast<size_t>(S) * rows * d * sizeof(float)) +
            round256(static_cast<size_t>(S) * rows * sizeof(float));
 }
-
-}  // namespace
-
-extern "C" {
-
-attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
-                     int N, int d, float scale, int causal, attn_stream_t stream) {
-    return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
-}
-
-attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                         int H, int Hk, int N, int d, float scale, int causal, attn_stream_t stream) {
-    return fwd_common(q, k, v, o, lse, B, H, Hk, N, d, scale, causal, stream);
-}
-
-size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
-    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
-    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
-    if (num_splits == 0) num_splits = kMaxSplits;  // enough for any automatic choice
-    return splitkv_bytes(B, H, N, d, num_splits);
-}
-
-attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
-                             void* workspace, int B, int H, int N, int d, float scale, int causal,
-                             int num_splits, attn_stream_t stream) {
-    attn_status rc = check_sizes(B, H, N, d, scale, causal);
-    if (rc != ATTN_OK) return rc;
-    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
-        return ATTN_ERR_INVALID;
-    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return ATTN_ERR_INVALID;
-    DeviceState* ds = nullptr;
-    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-    const int BH = B * H;
-    const int n_kv = (N + kTile - 1) / kTile;
-    int S = num_splits;
-    if (S == 0) {
-        int dev = 0, sms = 148;
-        if (cudaGetDevice(&dev) == cudaSuccess)
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        S = auto_splits(BH, N, sms);
-    }
-    if (S > n_kv) S = n_kv;
-    const int split_len = (n_kv + S - 1) / S;
-    S = (n_kv + split_len - 1) / split_len;  // no empty trailing split
-    if (S <= 1) return fwd_common(q, k, v, o, lse, B, H, H, N, d, scale, causal, stream);
-
-    CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, q, false, d, N, BH) || !make_map(&tk, k, false, d, N, BH) ||
-        !make_map(&tv, v, false, d, N, BH))
-        return ATTN_ERR_CUDA;
-    uint8_t* ws = static_cast<uint8_t*>(workspace);
-    const size_t rows = static_cast<size_t>(BH) * N;
-    FwdParams p;
-    p.o = o;
-    p.lse = lse;
-    p.N = N;
-    p.BH = BH;
-    p.H = H;
-    p.Hk = H;
-    p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
-    p.causal = causal;
-    p.win_left = -1;
-    p.win_right = causal ? 0 : -1;
-    p.cs = scale * 1.44269504088896340736f;
-    p.out_scale = 1.f;
-    p.n_splits = S;
-    p.split_len = split_len;
-    p.o_part = reinterpret_cast<float*>(ws);
-    p.lse_part = reinterpret_cast<float*>(ws + round256(static_cast<size_t>(S) * rows * d * sizeof(float)));
-    p.st = dev_status(ds);
-    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_fwd_bf16(d, tq, tk, tv, p, st) != cudaSuccess) return ATTN_ERR_CUDA;
-    CombineParams c;
-    c.o_part = p.o_part;
-    c.lse_part = p.lse_part;
-    c.o = o;
-    c.lse = lse;
-    c.S = S;
-    c.BH = BH;
-    c.N = N;
-    c.D = d;
-    return launch_splitkv_combine(c, st) == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
-}
-
-attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float sq, float sk, float sv,
-                         void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
-                         attn_stream_t stream) {
-    attn_status rc = check_sizes(B, H, N, d, scale, causal);
-    if (rc != ATTN_OK) return rc;
-    if (d != 128) return ATTN_ERR_UNSUPPORTED;
-    for (float s : {sq, sk, sv})
-        if (!(s > 0.f) || !std::isfinite(s)) return ATTN_ERR_INVALID;
-    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
-        return ATTN_ERR_INVALID;
-    DeviceState* ds = nullptr;
-    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
-    const int BH = B * H;
-    CUtensorMap tq, tk, tv;
-    if (!make_map(&tq, q8, true, d, N, BH) || !make_map(&tk, k8, true, d, N, BH) ||
-        !make_map(&tv, v8, true, d, N, BH))
-        return ATTN_ERR_CUDA;
-    FwdParams p;
-    p.o = o;
-    p.lse = lse;
-    p.N = N;
-    p.BH = BH;
-    p.H = H;
-    p.Hk = H;
-    p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
-    p.causal = causal;
-    p.win_left = -1;
-    p.win_right = causal ? 0 : -1;
-    p.cs = scale * sq * sk * 1.44269504088896340736f;
-    p.out_scale = sv;
-    p.n_splits = 1;
-    p.split_len = (N + kTile - 1) / kTile;
-    p.o_part = nullptr;
-    p.lse_part = nullptr;
-    p.st = dev_status(ds);
-    return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-               ? ATTN_OK
-               : ATTN_ERR_CUDA;
-}
-
-size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
-    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
-    return bwd_layout(B, H, N, d).total;
-}
-
-namespace {
 
 // Validated view of the backward workspace.
 struct BwdCall {
@@ -407,18 +297,20 @@ attn_status bwd_prepare(void* workspace, int B, int H, int N, int d, float scale
     return ATTN_OK;
 }
 
-}  // namespace
-
-attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
-                                int B, int H, int N, int d, attn_stream_t stream) {
+attn_status bwd_pre_run(const void* o, const Strides& os, const void* dout, const Strides& dos,
+                        const float* lse, void* workspace, int B, int H, int N, int d,
+                        attn_stream_t stream) {
     for (const void* p : {o, dout, static_cast<const void*>(lse)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
+    if (!strides_ok(os, 2) || !strides_ok(dos, 2)) return ATTN_ERR_INVALID;
     BwdCall c;
     attn_status rc = bwd_prepare(workspace, B, H, N, d, 1.f, 0, &c);
     if (rc != ATTN_OK) return rc;
     BwdPreParams pp;
     pp.o = o;
     pp.dout = dout;
+    pp.os = os;
+    pp.dos = dos;
     pp.lse = lse;
     pp.dq_acc = c.dq_acc;
     pp.lse2 = c.lse2;
@@ -426,32 +318,30 @@ attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* ls
     pp.N = N;
     pp.Npad = c.Np;
     pp.BH = c.BH;
+    pp.H = H;
     pp.D = d;
     return launch_bwd_pre(pp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? ATTN_OK
                                                                                      : ATTN_ERR_CUDA;
 }
 
-}  // extern "C"
-
-namespace {
-
-attn_status bwd_main_common(const void* q, const void* k, const void* v, const void* dout, void* dk,
-                            void* dv, void* workspace, int B, int H, int Hk, int N, int d, float scale,
-                            int causal, attn_stream_t stream, int win_left = -2,
-                            int win_right = -2) {
-    if (win_left == -2) {
-        win_left = -1;
-        win_right = causal ? 0 : -1;
-    }
+attn_status bwd_main_run(const void* q, const Strides& qs, const void* k, const Strides& ks,
+                         const void* v, const Strides& vs, const void* dout, const Strides& dos,
+                         void* dk, const Strides& dks, void* dv, const Strides& dvs, void* workspace,
+                         int B, int H, int Hk, int N, int d, float scale, int win_left, int win_right,
+                         attn_stream_t stream) {
     for (const void* p : {q, k, v, dout, static_cast<const void*>(dk), static_cast<const void*>(dv)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
-    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
+    for (const Strides* st : {&qs, &ks, &vs, &dos, &dks, &dvs})
+        if (!strides_ok(*st, 2)) return ATTN_ERR_INVALID;
+    attn_status rc;
+    if ((rc = check_group(H, Hk)) != ATTN_OK || (rc = check_window(win_left, win_right)) != ATTN_OK)
+        return rc;
+    const int causal = (win_left == -1 && win_right == 0) ? 1 : 0;
     BwdCall c;
-    attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, causal, &c);
-    if (rc != ATTN_OK) return rc;
+    if ((rc = bwd_prepare(workspace, B, H, N, d, scale, causal, &c)) != ATTN_OK) return rc;
     CUtensorMap tq, tk, tv, tdo, tdq;
-    if (!make_map(&tq, q, false, d, N, c.BH) || !make_map(&tk, k, false, d, N, B * Hk) ||
-        !make_map(&tv, v, false, d, N, B * Hk) || !make_map(&tdo, dout, false, d, N, c.BH) ||
+    if (!make_map(&tq, q, false, d, N, H, B, qs) || !make_map(&tk, k, false, d, N, Hk, B, ks) ||
+        !make_map(&tv, v, false, d, N, Hk, B, vs) || !make_map(&tdo, dout, false, d, N, H, B, dos) ||
         !make_map_acc(&tdq, c.dq_acc, d, c.Np, c.BH))
         return ATTN_ERR_CUDA;
     BwdParams bp;
@@ -460,6 +350,8 @@ attn_status bwd_main_common(const void* q, const void* k, const void* v, const v
     bp.dq_acc = c.dq_acc;
     bp.dk = dk;
     bp.dv = dv;
+    bp.dks = dks;
+    bp.dvs = dvs;
     bp.N = N;
     bp.Npad = c.Np;
     bp.BHk = B * Hk;
@@ -478,28 +370,20 @@ attn_status bwd_main_common(const void* q, const void* k, const void* v, const v
                : ATTN_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
-                          void* dv, void* workspace, int B, int H, int N, int d, float scale,
-                          int causal, attn_stream_t stream) {
-    return bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, H, N, d, scale, causal, stream);
-}
-
-attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, int d, float scale,
-                                attn_stream_t stream) {
-    if (!aligned16(dq)) return ATTN_ERR_INVALID;
+attn_status dq_convert_run(void* dq, const Strides& dqs, void* workspace, int B, int H, int N, int d,
+                           float scale, attn_stream_t stream) {
+    if (!aligned16(dq) || !strides_ok(dqs, 2)) return ATTN_ERR_INVALID;
     BwdCall c;
     attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, 0, &c);
     if (rc != ATTN_OK) return rc;
     DqConvertParams cp;
     cp.dq_acc = c.dq_acc;
     cp.dq = dq;
+    cp.dqs = dqs;
     cp.N = N;
     cp.Npad = c.Np;
     cp.BH = c.BH;
+    cp.H = H;
     cp.D = d;
     cp.scale = scale;
     return launch_dq_convert(cp, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -507,72 +391,252 @@ attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, 
                : ATTN_ERR_CUDA;
 }
 
-attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
-                     const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
-                     int N, int d, float scale, int causal, attn_stream_t stream) {
-    // Validate everything before the first launch so that a bad argument
-    // leaves the stream untouched.
+// The whole backward: everything is validated before the first launch, so a
+// bad argument leaves the stream untouched.
+attn_status bwd_run(const void* q, const Strides& qs, const void* k, const Strides& ks, const void* v,
+                    const Strides& vs, const void* o, const Strides& os, const void* dout,
+                    const Strides& dos, const float* lse, void* dq, const Strides& dqs, void* dk,
+                    const Strides& dks, void* dv, const Strides& dvs, void* workspace, int B, int H,
+                    int Hk, int N, int d, float scale, int win_left, int win_right,
+                    attn_stream_t stream) {
+    const int causal = (win_left == -1 && win_right == 0) ? 1 : 0;
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
+    if ((rc = check_group(H, Hk)) != ATTN_OK || (rc = check_window(win_left, win_right)) != ATTN_OK)
+        return rc;
     for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
                           static_cast<const void*>(dk), static_cast<const void*>(dv)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
+    for (const Strides* st : {&qs, &ks, &vs, &os, &dos, &dqs, &dks, &dvs})
+        if (!strides_ok(*st, 2)) return ATTN_ERR_INVALID;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return ATTN_ERR_INVALID;
-    if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
-    if ((rc = attn_bwd_main(q, k, v, dout, dk, dv, workspace, B, H, N, d, scale, causal, stream)) !=
+    if ((rc = bwd_pre_run(o, os, dout, dos, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
+    if ((rc = bwd_main_run(q, qs, k, ks, v, vs, dout, dos, dk, dks, dv, dvs, workspace, B, H, Hk, N, d,
+                           scale, win_left, win_right, stream)) != ATTN_OK)
+        return rc;
+    return dq_convert_run(dq, dqs, workspace, B, H, N, d, scale, stream);
+}
+
+Strides from_abi(const attn_strides_t& s) {
+    Strides r;
+    r.b = s.b;
+    r.h = s.h;
+    r.n = s.n;
+    return r;
+}
+
+}  // namespace
+
+cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream) {
+    wait_selftest_kernel<<<1, 64, 0, stream>>>(st);
+    return cudaGetLastError();
+}
+
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int H,
+                     int N, int d, float scale, int causal, attn_stream_t stream) {
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    const Strides ds = dense(H, N, d);
+    return fwd_run(q, ds, k, ds, v, ds, o, ds, lse, B, H, H, N, d, scale, -1, causal ? 0 : -1, stream);
+}
+
+attn_status attn_fwd_gqa(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                         int H, int Hk, int N, int d, float scale, int causal, attn_stream_t stream) {
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (check_group(H, Hk) != ATTN_OK) return ATTN_ERR_INVALID;
+    const Strides qs = dense(H, N, d), ks = dense(Hk, N, d);
+    return fwd_run(q, qs, k, ks, v, ks, o, qs, lse, B, H, Hk, N, d, scale, -1, causal ? 0 : -1, stream);
+}
+
+attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                            int H, int Hk, int N, int d, float scale, int window_left,
+                            int window_right, attn_stream_t stream) {
+    if (check_group(H, Hk) != ATTN_OK) return ATTN_ERR_INVALID;
+    const Strides qs = dense(H, N, d), ks = dense(Hk, N, d);
+    return fwd_run(q, qs, k, ks, v, ks, o, qs, lse, B, H, Hk, N, d, scale, window_left, window_right,
+                   stream);
+}
+
+attn_status attn_fwd_strided(const void* q, attn_strides_t qs, const void* k, attn_strides_t ks,
+                             const void* v, attn_strides_t vs, void* o, attn_strides_t os, float* lse,
+                             int B, int H, int Hk, int N, int d, float scale, int window_left,
+                             int window_right, attn_stream_t stream) {
+    return fwd_run(q, from_abi(qs), k, from_abi(ks), v, from_abi(vs), o, from_abi(os), lse, B, H, Hk,
+                   N, d, scale, window_left, window_right, stream);
+}
+
+size_t attn_fwd_splitkv_workspace_bytes(int B, int H, int N, int d, int num_splits) {
+    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
+    if (num_splits < 0 || num_splits > kMaxSplits) return 0;
+    if (num_splits == 0) num_splits = kMaxSplits;  // enough for any automatic choice
+    return splitkv_bytes(B, H, N, d, num_splits);
+}
+
+attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                             void* workspace, int B, int H, int N, int d, float scale, int causal,
+                             int num_splits, attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (num_splits < 0 || num_splits > kMaxSplits) return ATTN_ERR_INVALID;
+    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return ATTN_ERR_INVALID;
+    const int BH = B * H;
+    const int n_kv = (N + kTile - 1) / kTile;
+    int S = num_splits;
+    if (S == 0) {
+        int dev = 0, sms = 148;
+        if (cudaGetDevice(&dev) == cudaSuccess)
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        S = auto_splits(BH, N, sms);
+    }
+    if (S > n_kv) S = n_kv;
+    const Strides ds = dense(H, N, d);
+    const int wr = causal ? 0 : -1;
+    if (S <= 1) return fwd_run(q, ds, k, ds, v, ds, o, ds, lse, B, H, H, N, d, scale, -1, wr, stream);
+    SplitArgs sp;
+    sp.split_len = (n_kv + S - 1) / S;
+    sp.n_splits = (n_kv + sp.split_len - 1) / sp.split_len;  // no empty trailing split
+    const size_t rows = static_cast<size_t>(BH) * N;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    sp.o_part = reinterpret_cast<float*>(ws);
+    sp.lse_part = reinterpret_cast<float*>(
+        ws + round256(static_cast<size_t>(sp.n_splits) * rows * d * sizeof(float)));
+    if ((rc = fwd_run(q, ds, k, ds, v, ds, o, ds, lse, B, H, H, N, d, scale, -1, wr, stream, sp)) !=
         ATTN_OK)
         return rc;
-    return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
+    CombineParams c;
+    c.o_part = sp.o_part;
+    c.lse_part = sp.lse_part;
+    c.o = o;
+    c.os = ds;
+    c.lse = lse;
+    c.S = sp.n_splits;
+    c.BH = BH;
+    c.H = H;
+    c.N = N;
+    c.D = d;
+    return launch_splitkv_combine(c, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float sq, float sk, float sv,
+                         void* o, float* lse, int B, int H, int N, int d, float scale, int causal,
+                         attn_stream_t stream) {
+    attn_status rc = check_sizes(B, H, N, d, scale, causal);
+    if (rc != ATTN_OK) return rc;
+    if (d != 128) return ATTN_ERR_UNSUPPORTED;
+    for (float s : {sq, sk, sv})
+        if (!(s > 0.f) || !std::isfinite(s)) return ATTN_ERR_INVALID;
+    if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
+        return ATTN_ERR_INVALID;
+    DeviceState* ds = nullptr;
+    if ((rc = device_state(&ds)) != ATTN_OK) return rc;
+    const Strides st = dense(H, N, d);
+    CUtensorMap tq, tk, tv;
+    if (!make_map(&tq, q8, true, d, N, H, B, st) || !make_map(&tk, k8, true, d, N, H, B, st) ||
+        !make_map(&tv, v8, true, d, N, H, B, st))
+        return ATTN_ERR_CUDA;
+    FwdParams p;
+    p.o = o;
+    p.os = st;
+    p.lse = lse;
+    p.N = N;
+    p.BH = B * H;
+    p.H = H;
+    p.Hk = H;
+    p.n_pairs = (N + 2 * kTile - 1) / (2 * kTile);
+    p.causal = causal;
+    p.win_left = -1;
+    p.win_right = causal ? 0 : -1;
+    p.cs = scale * sq * sk * 1.44269504088896340736f;
+    p.out_scale = sv;
+    p.n_splits = 1;
+    p.split_len = (N + kTile - 1) / kTile;
+    p.o_part = nullptr;
+    p.lse_part = nullptr;
+    p.st = dev_status(ds);
+    return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? ATTN_OK
+               : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
+    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
+    return bwd_layout(B, H, N, d).total;
+}
+
+attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
+                                int B, int H, int N, int d, attn_stream_t stream) {
+    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return check_sizes(B, H, N, d, 1.f, 0);
+    const Strides ds = dense(H, N, d);
+    return bwd_pre_run(o, ds, dout, ds, lse, workspace, B, H, N, d, stream);
+}
+
+attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
+                          void* dv, void* workspace, int B, int H, int N, int d, float scale,
+                          int causal, attn_stream_t stream) {
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (check_sizes(B, H, N, d, scale, causal) != ATTN_OK) return check_sizes(B, H, N, d, scale, causal);
+    const Strides ds = dense(H, N, d);
+    return bwd_main_run(q, ds, k, ds, v, ds, dout, ds, dk, ds, dv, ds, workspace, B, H, H, N, d, scale,
+                        -1, causal ? 0 : -1, stream);
+}
+
+attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, int d, float scale,
+                                attn_stream_t stream) {
+    if (check_sizes(B, H, N, d, scale, 0) != ATTN_OK) return check_sizes(B, H, N, d, scale, 0);
+    return dq_convert_run(dq, dense(H, N, d), workspace, B, H, N, d, scale, stream);
+}
+
+attn_status attn_bwd(const void* q, const void* k, const void* v, const void* o, const void* dout,
+                     const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H,
+                     int N, int d, float scale, int causal, attn_stream_t stream) {
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (check_sizes(B, H, N, d, scale, causal) != ATTN_OK) return check_sizes(B, H, N, d, scale, causal);
+    const Strides ds = dense(H, N, d);
+    return bwd_run(q, ds, k, ds, v, ds, o, ds, dout, ds, lse, dq, ds, dk, ds, dv, ds, workspace, B, H,
+                   H, N, d, scale, -1, causal ? 0 : -1, stream);
 }
 
 attn_status attn_bwd_gqa(const void* q, const void* k, const void* v, const void* o,
                          const void* dout, const float* lse, void* dq, void* dk, void* dv,
                          void* workspace, int B, int H, int Hk, int N, int d, float scale, int causal,
                          attn_stream_t stream) {
-    attn_status rc = check_sizes(B, H, N, d, scale, causal);
-    if (rc != ATTN_OK) return rc;
-    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
-    for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
-                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
-        if (!aligned16(p)) return ATTN_ERR_INVALID;
-    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return ATTN_ERR_INVALID;
-    if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
-    if ((rc = bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, Hk, N, d, scale, causal,
-                              stream)) != ATTN_OK)
-        return rc;
-    return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
-}
-
-attn_status attn_fwd_window(const void* q, const void* k, const void* v, void* o, float* lse, int B,
-                            int H, int Hk, int N, int d, float scale, int window_left,
-                            int window_right, attn_stream_t stream) {
-    if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID;
-    const int causal = (window_left == -1 && window_right == 0) ? 1 : 0;
-    return fwd_common(q, k, v, o, lse, B, H, Hk, N, d, scale, causal, stream, window_left,
-                      window_right);
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    if (check_group(H, Hk) != ATTN_OK) return ATTN_ERR_INVALID;
+    if (check_sizes(B, H, N, d, scale, causal) != ATTN_OK) return check_sizes(B, H, N, d, scale, causal);
+    const Strides qs = dense(H, N, d), ks = dense(Hk, N, d);
+    return bwd_run(q, qs, k, ks, v, ks, o, qs, dout, qs, lse, dq, qs, dk, ks, dv, ks, workspace, B, H,
+                   Hk, N, d, scale, -1, causal ? 0 : -1, stream);
 }
 
 attn_status attn_bwd_window(const void* q, const void* k, const void* v, const void* o,
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             void* workspace, int B, int H, int Hk, int N, int d, float scale,
                             int window_left, int window_right, attn_stream_t stream) {
-    if (window_left < -1 || window_right < -1) return ATTN_ERR_INVALID;
-    const int causal = (window_left == -1 && window_right == 0) ? 1 : 0;
-    attn_status rc = check_sizes(B, H, N, d, scale, causal);
-    if (rc != ATTN_OK) return rc;
-    if (Hk < 1 || Hk > H || H % Hk != 0) return ATTN_ERR_INVALID;
-    for (const void* p : {q, k, v, o, dout, static_cast<const void*>(lse), static_cast<const void*>(dq),
-                          static_cast<const void*>(dk), static_cast<const void*>(dv)})
-        if (!aligned16(p)) return ATTN_ERR_INVALID;
-    if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
-        return ATTN_ERR_INVALID;
-    if ((rc = attn_bwd_preprocess(o, dout, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
-    if ((rc = bwd_main_common(q, k, v, dout, dk, dv, workspace, B, H, Hk, N, d, scale, causal, stream,
-                              window_left, window_right)) != ATTN_OK)
-        return rc;
-    return attn_bwd_dq_convert(dq, workspace, B, H, N, d, scale, stream);
+    if (check_group(H, Hk) != ATTN_OK) return ATTN_ERR_INVALID;
+    if (check_sizes(B, H, N, d, scale, 0) != ATTN_OK) return check_sizes(B, H, N, d, scale, 0);
+    const Strides qs = dense(H, N, d), ks = dense(Hk, N, d);
+    return bwd_run(q, qs, k, ks, v, ks, o, qs, dout, qs, lse, dq, qs, dk, ks, dv, ks, workspace, B, H,
+                   Hk, N, d, scale, window_left, window_right, stream);
+}
+
+attn_status attn_bwd_strided(const void* q, attn_strides_t qs, const void* k, attn_strides_t ks,
+                             const void* v, attn_strides_t vs, const void* o, attn_strides_t os,
+                             const void* dout, attn_strides_t dos, const float* lse, void* dq,
+                             attn_strides_t dqs, void* dk, attn_strides_t dks, void* dv,
+                             attn_strides_t dvs, void* workspace, int B, int H, int Hk, int N, int d,
+                             float scale, int window_left, int window_right, attn_stream_t stream) {
+    return bwd_run(q, from_abi(qs), k, from_abi(ks), v, from_abi(vs), o, from_abi(os), dout,
+                   from_abi(dos), lse, dq, from_abi(dqs), dk, from_abi(dks), dv, from_abi(dvs),
+                   workspace, B, H, Hk, N, d, scale, window_left, window_right, stream);
 }
 
 attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site) {

@@ -84,63 +84,86 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
 // ---------------------------------------------------------------------------
-// 1. preprocess: one warp per (head, row) of the padded row range
+// 1. preprocess: one block per kAuxRows consecutive rows of one head
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdPreParams p) {
-    const int lane = threadIdx.x & 31;
-    const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
-    const long long rows = static_cast<long long>(p.BH) * p.Npad;
-    const int epl = p.D / 32;  // bf16 elements per lane (2 or 4)
-    for (long long r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += warps) {
-        const int bh = static_cast<int>(r / p.Npad);
-        const int n = static_cast<int>(r % p.Npad);
-        float acc = 0.f;
-        if (n < p.N) {
-            const size_t base = (static_cast<size_t>(bh) * p.N + n) * p.D + lane * epl;
-            const uint16_t* o16 = static_cast<const uint16_t*>(p.o) + base;
-            const uint16_t* d16 = static_cast<const uint16_t*>(p.dout) + base;
-            if (epl == 4) {
-                const uint2 a = *reinterpret_cast<const uint2*>(o16);
-                const uint2 b = *reinterpret_cast<const uint2*>(d16);
-                acc = bf16lo(a.x) * bf16lo(b.x) + bf16hi(a.x) * bf16hi(b.x) +
-                      bf16lo(a.y) * bf16lo(b.y) + bf16hi(a.y) * bf16hi(b.y);
-            } else {
-                const uint32_t a = *reinterpret_cast<const uint32_t*>(o16);
-                const uint32_t b = *reinterpret_cast<const uint32_t*>(d16);
-                acc = bf16lo(a) * bf16lo(b) + bf16hi(a) * bf16hi(b);
-            }
-        }
+// Both auxiliary kernels give each row D/8 threads (8 elements, one 16-byte
+// load per thread), so a warp covers 2 (D = 128) or 4 (D = 64) rows and the
+// row sum is a shuffle reduction over D/8 lanes.  Npad is a multiple of 128,
+// so a block never straddles two heads and the head index is one division per
+// block.
+constexpr int kAuxRows = 64;
+constexpr int kAuxThreads = 256;
+
+template <int D>
+__global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdPreParams p) {
+    constexpr int TPR = D / 8;                   // threads per row
+    constexpr int RPP = kAuxThreads / TPR;       // rows per pass
+    constexpr int PASSES = kAuxRows / RPP;
+    const int blocks_per_head = p.Npad / kAuxRows;
+    const int bh = static_cast<int>(blockIdx.x / blocks_per_head);
+    const int n0 = static_cast<int>(blockIdx.x % blocks_per_head) * kAuxRows;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int c = threadIdx.x % TPR, rr = threadIdx.x / TPR;
+    const uint16_t* obase = static_cast<const uint16_t*>(p.o) + b * p.os.b + h * p.os.h + c * 8;
+    const uint16_t* dbase = static_cast<const uint16_t*>(p.dout) + b * p.dos.b + h * p.dos.h + c * 8;
+    uint4 a[PASSES], g[PASSES];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-        if (lane == 0) {
+    for (int k = 0; k < PASSES; ++k) {
+        const int n = n0 + k * RPP + rr;
+        a[k] = g[k] = make_uint4(0u, 0u, 0u, 0u);
+        if (n < p.N) {
+            a[k] = *reinterpret_cast<const uint4*>(obase + n * p.os.n);
+            g[k] = *reinterpret_cast<const uint4*>(dbase + n * p.dos.n);
+        }
+    }
+    // Zero this block's rows of the dQ accumulator (contiguous, fp32 [BH, Npad, D]).
+    float4* z = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.Npad + n0) * D);
+#pragma unroll
+    for (int k = threadIdx.x; k < kAuxRows * D / 4; k += kAuxThreads)
+        z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < PASSES; ++k) {
+        const int n = n0 + k * RPP + rr;
+        float acc = bf16lo(a[k].x) * bf16lo(g[k].x) + bf16hi(a[k].x) * bf16hi(g[k].x) +
+                    bf16lo(a[k].y) * bf16lo(g[k].y) + bf16hi(a[k].y) * bf16hi(g[k].y) +
+                    bf16lo(a[k].z) * bf16lo(g[k].z) + bf16hi(a[k].z) * bf16hi(g[k].z) +
+                    bf16lo(a[k].w) * bf16lo(g[k].w) + bf16hi(a[k].w) * bf16hi(g[k].w);
+#pragma unroll
+        for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (c == 0) {
             const size_t v = static_cast<size_t>(bh) * p.Npad + n;
             p.dsum[v] = acc;
             p.lse2[v] = n < p.N ? -p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e : -INFINITY;
         }
-        float4* z = reinterpret_cast<float4*>(p.dq_acc + r * p.D);
-        for (int c = lane; c < p.D / 4; c += 32) z[c] = make_float4(0.f, 0.f, 0.f, 0.f);
     }
 }
 
 // ---------------------------------------------------------------------------
-// 3. dQ conversion: 8 elements per thread
+// 3. dQ conversion: one block per kAuxRows rows of one head, 8 elements a thread
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) dq_convert_kernel(const DqConvertParams p) {
-    const long long total = static_cast<long long>(p.BH) * p.N * (p.D / 8);
-    const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
-    for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < total;
-         t += stride) {
-        const long long row = t / (p.D / 8);  // bh * N + n
-        const int c8 = static_cast<int>(t % (p.D / 8));
-        const int bh = static_cast<int>(row / p.N);
-        const int n = static_cast<int>(row % p.N);
-        const float4* src = reinterpret_cast<const float4*>(
-            p.dq_acc + (static_cast<size_t>(bh) * p.Npad + n) * p.D + c8 * 8);
-        const float4 a = src[0], b = src[1];
-        const float s = p.scale;
-        uint32_t w0 = pack_bf16x2(a.x * s, a.y * s), w1 = pack_bf16x2(a.z * s, a.w * s);
-        uint32_t w2 = pack_bf16x2(b.x * s, b.y * s), w3 = pack_bf16x2(b.z * s, b.w * s);
-        st_global_v4(static_cast<uint16_t*>(p.dq) + row * p.D + c8 * 8, w0, w1, w2, w3);
+template <int D>
+__global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const DqConvertParams p) {
+    constexpr int TPR = D / 8;
+    constexpr int RPP = kAuxThreads / TPR;
+    constexpr int PASSES = kAuxRows / RPP;
+    const int blocks_per_head = p.Npad / kAuxRows;
+    const int bh = static_cast<int>(blockIdx.x / blocks_per_head);
+    const int n0 = static_cast<int>(blockIdx.x % blocks_per_head) * kAuxRows;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int c = threadIdx.x % TPR, rr = threadIdx.x / TPR;
+    const float* src = p.dq_acc + (static_cast<size_t>(bh) * p.Npad + n0 + rr) * D + c * 8;
+    uint16_t* dst = static_cast<uint16_t*>(p.dq) + b * p.dqs.b + h * p.dqs.h + c * 8;
+    const float s = p.scale;
+#pragma unroll
+    for (int k = 0; k < PASSES; ++k) {
+        const int n = n0 + k * RPP + rr;
+        if (n < p.N) {
+            const float4* f = reinterpret_cast<const float4*>(src + k * RPP * D);
+            const float4 x = f[0], y = f[1];
+            st_global_v4(dst + static_cast<long long>(n) * p.dqs.n, pack_bf16x2(x.x * s, x.y * s),
+                         pack_bf16x2(x.z * s, x.w * s), pack_bf16x2(y.x * s, y.y * s),
+                         pack_bf16x2(y.z * s, y.w * s));
+        }
     }
 }
 
@@ -204,6 +227,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // visited one after the other; dK and dV accumulate over all of them.
     const int G = prm.H / prm.Hk;
     const int q_bh0 = (kv_bh / prm.Hk) * prm.H + (kv_bh % prm.Hk) * G;
+    const int b_idx = kv_bh / prm.Hk, hk_idx = kv_bh % prm.Hk;  // batch, key/value head
+    const int bH0 = b_idx * prm.H;  // query head of (batch, head) index bh is bh - bH0
     const int n_steps = G * n_qh;
     // Query tile of step t.  Over the full range each key tile starts at its
     // own index and wraps, so CTAs that run together reduce into different dQ
@@ -254,10 +279,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
             for (int blk = 0; blk < T::NBLK; ++blk) {
-                tma_load_3d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
-                            kv_bh);
-                tma_load_3d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
-                            kv_bh);
+                tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
+                            hk_idx, b_idx);
+                tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
+                            hk_idx, b_idx);
             }
             int t = 0;
             int tt = 0, bh = q_bh0;  // step t = (head bh - q_bh0) * n_qh + tt
@@ -275,10 +300,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint32_t bf = b_qdo_full(s);
                 mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
                 for (int blk = 0; blk < T::NBLK; ++blk) {
-                    tma_load_3d(sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_q, bf,
-                                blk * 64, i * kTile, bh);
-                    tma_load_3d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
-                                blk * 64, i * kTile, bh);
+                    tma_load_4d(sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_q, bf,
+                                blk * 64, i * kTile, bh - bH0, b_idx);
+                    tma_load_4d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
+                                blk * 64, i * kTile, bh - bH0, b_idx);
                 }
                 const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile;
                 bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
@@ -460,7 +485,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (ok && wait_warp(b_dkv_full, 0, abort_flag, prm.st, SITE_DKV)) {
             tc_fence_after();
             const bool row_ok = kv_row < N;
-            const size_t roff = (static_cast<size_t>(kv_bh) * N + (row_ok ? kv_row : 0)) * D * 2;
+            const Strides& ds = h ? prm.dks : prm.dvs;
+            const long long roff = (b_idx * ds.b + hk_idx * ds.h + (row_ok ? kv_row : 0) * ds.n) * 2;
             const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
             uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
             const float f = h ? prm.scale : 1.f;
@@ -594,18 +620,22 @@ cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, c
 }  // namespace
 
 cudaError_t launch_bwd_pre(const BwdPreParams& p, cudaStream_t stream) {
-    const long long rows = static_cast<long long>(p.BH) * p.Npad;
-    const long long blocks = (rows + 7) / 8;
-    const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
-    bwd_pre_kernel<<<grid, 256, 0, stream>>>(p);
+    if (p.Npad % kAuxRows != 0) return cudaErrorInvalidValue;
+    const long long blocks = static_cast<long long>(p.BH) * (p.Npad / kAuxRows);
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+    if (p.D == 64) bwd_pre_kernel<64><<<static_cast<unsigned>(blocks), kAuxThreads, 0, stream>>>(p);
+    else if (p.D == 128) bwd_pre_kernel<128><<<static_cast<unsigned>(blocks), kAuxThreads, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
-    const long long total = static_cast<long long>(p.BH) * p.N * (p.D / 8);
-    const long long blocks = (total + 255) / 256;
-    const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
-    dq_convert_kernel<<<grid, 256, 0, stream>>>(p);
+    if (p.Npad % kAuxRows != 0) return cudaErrorInvalidValue;
+    const long long blocks = static_cast<long long>(p.BH) * (p.Npad / kAuxRows);
+    if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
+    if (p.D == 64) dq_convert_kernel<64><<<static_cast<unsigned>(blocks), kAuxThreads, 0, stream>>>(p);
+    else if (p.D == 128) dq_convert_kernel<128><<<static_cast<unsigned>(blocks), kAuxThreads, 0, stream>>>(p);
+    else return cudaErrorInvalidValue;
     return cudaGetLastError();
 }
 

@@ -142,7 +142,8 @@ __global__ void __launch_bounds__(320, 1)
     const int n_kv = (n_t[0] > 0 || n_t[1] > 0) ? kv_hi - kv_lo : 0;
     // Key/value head of this query head (grouped-query attention: H/Hk query
     // heads share one key/value head; Hk == H is ordinary multi-head attention).
-    const int kv_bh = (bh / prm.H) * prm.Hk + (bh % prm.H) / (prm.H / prm.Hk);
+    const int b_idx = bh / prm.H, h_idx = bh % prm.H;  // batch and query head
+    const int hk_idx = h_idx / (prm.H / prm.Hk);          // key/value head
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
@@ -181,8 +182,8 @@ __global__ void __launch_bounds__(320, 1)
             for (int g = 0; g < 2; ++g) {
                 if (n_t[g] == 0) continue;
                 for (int blk = 0; blk < T::NBLK; ++blk)
-                    tma_load_3d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
-                                blk * T::BLK_ELEMS, (2 * pair + g) * kTile, bh);
+                    tma_load_4d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
+                                blk * T::BLK_ELEMS, (2 * pair + g) * kTile, h_idx, b_idx);
             }
             int idx = 0;
             bool ok = true;
@@ -199,8 +200,9 @@ __global__ void __launch_bounds__(320, 1)
                     mbar_arrive_expect_tx(b_kv_full(slot), T::TILE_BYTES);
                     const CUtensorMap* map = t ? &tm_v : &tm_k;
                     for (int blk = 0; blk < T::NBLK; ++blk)
-                        tma_load_3d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
-                                    b_kv_full(slot), blk * T::BLK_ELEMS, (kv_lo + j) * kTile, kv_bh);
+                        tma_load_4d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
+                                    b_kv_full(slot), blk * T::BLK_ELEMS, (kv_lo + j) * kTile, hk_idx,
+                                    b_idx);
                 }
             }
             // Let every copy this thread started land before the CTA can exit.
@@ -546,7 +548,7 @@ __global__ void __launch_bounds__(320, 1)
             const float l_norm = FP8 ? l_sum : l_pv;
             const float inv_l = l_norm > 0.f ? prm.out_scale / l_norm : 0.f;
             uint8_t* orow = static_cast<uint8_t*>(prm.o) +
-                            (static_cast<size_t>(bh) * N + (row_ok ? q_row : 0)) * D * 2;
+                            (b_idx * prm.os.b + h_idx * prm.os.h + (row_ok ? q_row : 0) * prm.os.n) * 2;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -603,7 +605,9 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const CombineParam
             }
         }
         const float inv = wsum > 0.f ? 1.f / wsum : 0.f;
-        uint16_t* dst = static_cast<uint16_t*>(p.o) + r * p.D + lane * epl;
+        const long long bh = r / p.N, n = r % p.N;
+        uint16_t* dst = static_cast<uint16_t*>(p.o) + (bh / p.H) * p.os.b + (bh % p.H) * p.os.h +
+                        n * p.os.n + lane * epl;
         if (epl == 4) {
             const uint32_t w0 = pack_bf16x2(acc[0] * inv, acc[1] * inv);
             const uint32_t w1 = pack_bf16x2(acc[2] * inv, acc[3] * inv);

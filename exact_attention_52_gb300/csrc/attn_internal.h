@@ -11,8 +11,14 @@ namespace attn {
 
 constexpr int kTile = 128;  // rows of Q, K, V per tile (M and N of every MMA)
 
+// Element strides of a [B, heads, N, d] view whose d dimension is contiguous.
+struct Strides {
+    long long b, h, n;
+};
+
 struct FwdParams {
-    void* o;          // bf16 [BH, N, D]
+    void* o;          // bf16 [B, H, N, D] with strides os
+    Strides os;
     float* lse;       // fp32 [BH, N], natural log of the row normaliser
     int N;            // sequence length (queries = keys)
     int BH;           // batch * query heads
@@ -36,27 +42,30 @@ struct FwdParams {
 struct CombineParams {
     const float* o_part;    // fp32 [S, BH, N, D]
     const float* lse_part;  // fp32 [S, BH, N]
-    void* o;                // bf16 [BH, N, D]
+    void* o;                // bf16 [B, H, N, D] with strides os
+    Strides os;
     float* lse;             // fp32 [BH, N]
-    int S, BH, N, D;
+    int S, BH, H, N, D;
 };
 
 struct BwdPreParams {
-    const void* o;     // bf16 [BH, N, D]
-    const void* dout;  // bf16 [BH, N, D]
+    const void* o;     // bf16 [B, H, N, D] with strides os
+    const void* dout;  // bf16 [B, H, N, D] with strides dos
+    Strides os, dos;
     const float* lse;  // fp32 [BH, N]
     float* dq_acc;     // fp32 [BH, Npad, D], zeroed here
     float* lse2;       // fp32 [BH, Npad]: -LSE * log2(e); -inf on padding rows
     float* dsum;       // fp32 [BH, Npad]: D_i = sum_k dO_ik O_ik; 0 on padding rows
-    int N, Npad, BH, D;
+    int N, Npad, BH, H, D;
 };
 
 struct BwdParams {
     const float* lse2;  // workspace (-LSE * log2(e)), see BwdPreParams
     const float* dsum;
     float* dq_acc;
-    void* dk;           // bf16 [B*Hk, N, D]
-    void* dv;           // bf16 [B*Hk, N, D]
+    void* dk;           // bf16 [B, Hk, N, D] with strides dks
+    void* dv;           // bf16 [B, Hk, N, D] with strides dvs
+    Strides dks, dvs;
     int N, Npad;
     int BHk;            // batch * key/value heads: CTAs are (kv head, key tile)
     int H, Hk;          // query heads, key/value heads; each CTA loops over its H/Hk query heads
@@ -71,8 +80,9 @@ struct BwdParams {
 
 struct DqConvertParams {
     const float* dq_acc;  // fp32 [BH, Npad, D]
-    void* dq;             // bf16 [BH, N, D]
-    int N, Npad, BH, D;
+    void* dq;             // bf16 [B, H, N, D] with strides dqs
+    Strides dqs;
+    int N, Npad, BH, H, D;
     float scale;
 };
 

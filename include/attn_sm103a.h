@@ -44,6 +44,15 @@ extern "C" {
 
 typedef struct CUstream_st* attn_stream_t; /* same type as cudaStream_t */
 
+/* Element strides of a [B, heads, N, d] view whose d dimension is contiguous
+ * (stride 1).  A dense [B, heads, N, d] tensor has n = d, h = N*d,
+ * b = heads*N*d; PyTorch's [B, N, heads, d] layout has n = heads*d, h = d,
+ * b = N*heads*d.  Every stride times the element size must be a multiple of
+ * 16 bytes. */
+typedef struct {
+    int64_t b, h, n;
+} attn_strides_t;
+
 typedef enum {
     ATTN_OK = 0,
     ATTN_ERR_INVALID = -1,     /* bad pointer, size, alignment or scale */
@@ -195,6 +204,29 @@ attn_status attn_bwd_window(const void* q, const void* k, const void* v, const v
                             const void* dout, const float* lse, void* dq, void* dk, void* dv,
                             void* workspace, int B, int H, int Hk, int N, int d, float scale,
                             int window_left, int window_right, attn_stream_t stream);
+
+/*
+ * The general entry points: grouped heads, sliding window, and any strides
+ * per tensor (q, o, dout, dq over H heads; k, v, dk, dv over Hk heads).
+ * window_left / window_right as attn_fwd_window (-1, -1: no mask; -1, 0:
+ * causal).  lse stays dense [B, H, N].  Every other entry point is a special
+ * case of these two.  Strides that are negative, or not multiples of 16
+ * bytes, give ATTN_ERR_INVALID.
+ * Source: FlashAttention-3 walkthrough (batch / seqlen / num_heads /
+ * num_heads_k / head_dim runtime parameters); ai.engineer items on tensor
+ * storage, strides and views (the tensor is a view over storage given by its
+ * strides).
+ */
+attn_status attn_fwd_strided(const void* q, attn_strides_t qs, const void* k, attn_strides_t ks,
+                             const void* v, attn_strides_t vs, void* o, attn_strides_t os, float* lse,
+                             int B, int H, int Hk, int N, int d, float scale, int window_left,
+                             int window_right, attn_stream_t stream);
+attn_status attn_bwd_strided(const void* q, attn_strides_t qs, const void* k, attn_strides_t ks,
+                             const void* v, attn_strides_t vs, const void* o, attn_strides_t os,
+                             const void* dout, attn_strides_t dos, const float* lse, void* dq,
+                             attn_strides_t dqs, void* dk, attn_strides_t dks, void* dv,
+                             attn_strides_t dvs, void* workspace, int B, int H, int Hk, int N, int d,
+                             float scale, int window_left, int window_right, attn_stream_t stream);
 
 /*
  * FP8 forward pass: OCP E4M3 inputs with per-tensor fp32 scales.
