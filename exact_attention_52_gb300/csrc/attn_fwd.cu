@@ -213,14 +213,17 @@ __global__ void __launch_bounds__(320, 1)
         }
     } else if (warp == 9) {
         // ================= MMA issuer =================
-        if (lane == 0) {
+        // The whole warp walks the schedule (uniform control flow and operands);
+        // one elected lane issues each tcgen05 instruction.
+        __syncwarp();
+        {
             const uint32_t sq_base = smem_u32(sQ);
             const uint32_t skv_base = smem_u32(sKV);
             auto slot_addr = [&](int idx) {
                 return skv_base + static_cast<uint32_t>((idx % T::KV_SLOTS) * T::TILE_BYTES);
             };
             auto wait_kv = [&](int idx) {
-                return wait_one(b_kv_full(idx % T::KV_SLOTS), (idx / T::KV_SLOTS) & 1, abort_flag,
+                return wait_warp(b_kv_full(idx % T::KV_SLOTS), (idx / T::KV_SLOTS) & 1, abort_flag,
                                 prm.st, SITE_KV_FULL);
             };
             // S_g = Q_g K_j^T : both operands K-major, 32 bytes of K per instruction.
@@ -230,17 +233,17 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / T::UMMA_K; ++kk) {
                     const uint32_t off = (kk * 32) / 128 * T::BLK_BYTES + (kk * 32) % 128;
-                    mma_ss<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
+                    mma_ss_warp<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
                                 T::IDESC_S, kk > 0 ? 1u : 0u);
                 }
-                mma_commit(b_s_full + 8u * g);
+                mma_commit_warp(b_s_full + 8u * g);
             };
             // O_g += P_g V_j : P from tensor memory, V MN-major (rows = keys).
             auto issue_pv = [&](int g, int j, bool first) {
                 const uint32_t vb = slot_addr(2 * (j - kv_lo) + 1);
 #pragma unroll
                 for (int kk = 0; kk < kTile / T::UMMA_K; ++kk) {
-                    mma_ts<FP8>(tmem + (g ? T::COL_O1 : T::COL_O0),
+                    mma_ts_warp<FP8>(tmem + (g ? T::COL_O1 : T::COL_O0),
                                 tmem + (g ? T::COL_S1 : T::COL_S0) + kk * 8,
                                 sw128_desc(vb + kk * T::UMMA_K * 128, T::BLK_BYTES, 1024), T::IDESC_PV,
                                 (!first || kk > 0) ? 1u : 0u);
@@ -256,11 +259,11 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 if (n_t[0] > 0) issue_s(0, kv_lo);
                 if (n_t[1] > 0) issue_s(1, kv_lo);
-                mma_commit(b_kv_empty(0));
+                mma_commit_warp(b_kv_empty(0));
                 for (int j = 0; j < n_kv; ++j) {
                     bool v_ready = false, k_next_ready = false;
                     if (j < n_t[0]) {
-                        if (!wait_one(b_p_full, j & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                        if (!wait_warp(b_p_full, j & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
                         if (!wait_kv(2 * j + 1)) return false;
                         v_ready = true;
                         tc_fence_after();
@@ -271,32 +274,32 @@ __global__ void __launch_bounds__(320, 1)
                             tc_fence_after();
                             issue_s(0, kv_lo + j + 1);
                         } else {
-                            mma_commit(b_o_full);
+                            mma_commit_warp(b_o_full);
                         }
                     }
                     if (j < n_t[1]) {
-                        if (!wait_one(b_p_full + 8u, j & 1, abort_flag, prm.st, SITE_P_FULL))
+                        if (!wait_warp(b_p_full + 8u, j & 1, abort_flag, prm.st, SITE_P_FULL))
                             return false;
                         if (!v_ready && !wait_kv(2 * j + 1)) return false;
                         tc_fence_after();
                         issue_pv(1, kv_lo + j, j == 0);
                     }
-                    mma_commit(b_kv_empty((2 * j + 1) % T::KV_SLOTS));  // V_j consumed
+                    mma_commit_warp(b_kv_empty((2 * j + 1) % T::KV_SLOTS));  // V_j consumed
                     if (j < n_t[1]) {
                         if (j + 1 < n_t[1]) {
                             if (!k_next_ready && !wait_kv(2 * j + 2)) return false;
                             tc_fence_after();
                             issue_s(1, kv_lo + j + 1);
                         } else {
-                            mma_commit(b_o_full + 8u);
+                            mma_commit_warp(b_o_full + 8u);
                         }
                     }
-                    if (j + 1 < n_kv) mma_commit(b_kv_empty((2 * j + 2) % T::KV_SLOTS));  // K_{j+1}
+                    if (j + 1 < n_kv) mma_commit_warp(b_kv_empty((2 * j + 2) % T::KV_SLOTS));  // K_{j+1}
                 }
                 return true;
             };
             auto run = [&]() -> bool {
-                if (!wait_one(b_q, 0, abort_flag, prm.st, SITE_Q)) return false;
+                if (!wait_warp(b_q, 0, abort_flag, prm.st, SITE_Q)) return false;
                 if (n_kv == 0) return true;
                 if ((n_t[0] == 0 || lo_t[0] == kv_lo) && (n_t[1] == 0 || lo_t[1] == kv_lo))
                     return run_aligned();
@@ -304,7 +307,7 @@ __global__ void __launch_bounds__(320, 1)
                 tc_fence_after();
                 if (active(0, kv_lo)) issue_s(0, kv_lo);
                 if (active(1, kv_lo)) issue_s(1, kv_lo);
-                mma_commit(b_kv_empty(kidx(kv_lo) % T::KV_SLOTS));
+                mma_commit_warp(b_kv_empty(kidx(kv_lo) % T::KV_SLOTS));
                 for (int j = kv_lo; j < kv_lo + n_kv; ++j) {
                     const bool has_next = j + 1 < kv_lo + n_kv;
                     bool v_ready = false, k_next_ready = false;
@@ -316,7 +319,7 @@ __global__ void __launch_bounds__(320, 1)
                     };
                     // query tile 0: PV_0(j), then S_0(j+1)
                     if (active(0, j)) {
-                        if (!wait_one(b_p_full, (j - lo_t[0]) & 1, abort_flag, prm.st, SITE_P_FULL))
+                        if (!wait_warp(b_p_full, (j - lo_t[0]) & 1, abort_flag, prm.st, SITE_P_FULL))
                             return false;
                         if (!wait_kv(kidx(j) + 1)) return false;
                         v_ready = true;
@@ -327,7 +330,7 @@ __global__ void __launch_bounds__(320, 1)
                             tc_fence_after();
                             issue_s(0, j + 1);
                         } else {
-                            mma_commit(b_o_full);
+                            mma_commit_warp(b_o_full);
                         }
                     } else if (active(0, j + 1)) {
                         if (!need_k_next()) return false;
@@ -336,7 +339,7 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     // query tile 1: PV_1(j), release V_j, then S_1(j+1)
                     if (active(1, j)) {
-                        if (!wait_one(b_p_full + 8u, (j - lo_t[1]) & 1, abort_flag, prm.st, SITE_P_FULL))
+                        if (!wait_warp(b_p_full + 8u, (j - lo_t[1]) & 1, abort_flag, prm.st, SITE_P_FULL))
                             return false;
                         if (!v_ready && !wait_kv(kidx(j) + 1)) return false;
                         v_ready = true;
@@ -344,14 +347,14 @@ __global__ void __launch_bounds__(320, 1)
                         issue_pv(1, j, j == lo_t[1]);
                     }
                     if (!v_ready && !wait_kv(kidx(j) + 1)) return false;  // loaded, never used
-                    mma_commit(b_kv_empty((kidx(j) + 1) % T::KV_SLOTS));  // V_j consumed
+                    mma_commit_warp(b_kv_empty((kidx(j) + 1) % T::KV_SLOTS));  // V_j consumed
                     if (active(1, j)) {
                         if (active(1, j + 1)) {
                             if (!need_k_next()) return false;
                             tc_fence_after();
                             issue_s(1, j + 1);
                         } else {
-                            mma_commit(b_o_full + 8u);
+                            mma_commit_warp(b_o_full + 8u);
                         }
                     } else if (active(1, j + 1)) {
                         if (!need_k_next()) return false;
@@ -360,14 +363,14 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     if (has_next) {
                         if (!need_k_next()) return false;
-                        mma_commit(b_kv_empty(kidx(j + 1) % T::KV_SLOTS));  // K_{j+1} consumed
+                        mma_commit_warp(b_kv_empty(kidx(j + 1) % T::KV_SLOTS));  // K_{j+1} consumed
                     }
                 }
                 return true;
             };
             run();
             // Every MMA issued above must finish before tensor memory is freed.
-            mma_commit(b_done);
+            mma_commit_warp(b_done);
             wait_drain(b_done, 0, prm.st, SITE_DRAIN);
         }
     } else {
