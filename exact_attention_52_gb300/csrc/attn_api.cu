@@ -103,16 +103,16 @@ bool make_map(CUtensorMap* m, const void* base, bool fp8, int d, int N, int head
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D view {d, Npad, B*H} of the fp32 dQ accumulator; box {32, 128, 1}
-// (128 bytes x 128 rows), 128-byte swizzle, used for TMA reductions.
-bool make_map_acc(CUtensorMap* m, const float* base, int d, int Npad, int BH) {
+// 3-D view {d, Npad, B*H} of the fp32 dQ accumulator; box {32, box_rows, 1}
+// (128 bytes x box_rows rows), 128-byte swizzle, used for TMA reductions.
+bool make_map_acc(CUtensorMap* m, const float* base, int d, int Npad, int BH, int box_rows) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(Npad),
                                 static_cast<cuuint64_t>(BH)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(d) * 4,
                                    static_cast<cuuint64_t>(Npad) * d * 4};
-    const cuuint32_t box[3] = {32u, 128u, 1u};
+    const cuuint32_t box[3] = {32u, static_cast<cuuint32_t>(box_rows), 1u};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(base), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -342,7 +342,7 @@ attn_status bwd_main_run(const void* q, const Strides& qs, const void* k, const 
     CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_map(&tq, q, false, d, N, H, B, qs) || !make_map(&tk, k, false, d, N, Hk, B, ks) ||
         !make_map(&tv, v, false, d, N, Hk, B, vs) || !make_map(&tdo, dout, false, d, N, H, B, dos) ||
-        !make_map_acc(&tdq, c.dq_acc, d, c.Np, c.BH))
+        !make_map_acc(&tdq, c.dq_acc, d, c.Np, c.BH, d == 128 ? 64 : 128))
         return ATTN_ERR_CUDA;
     BwdParams bp;
     bp.lse2 = c.lse2;

@@ -16,19 +16,27 @@
 //  3. dq_convert  dQ = bf16(scale * accumulator)  (the second, combining
 //                 kernel of a split reduction, CUTLASS split-K item).
 //
-// bwd_main warp roles (320 threads):
-//   warps 0-3  compute: P^T, dS^T (one thread per key row); dK/dV epilogue
-//   warps 4-7  dQ writer: tensor memory -> red.global.add.v4.f32
-//   warp 8     TMA producer: K_j, V_j once; Q_i, dO_i, LSE2_i, D_i per step
-//   warp 9     MMA issuer
-// Tensor memory (lane = key row for S^T, dP^T, dV, dK; lane = query row for dQ):
-//   [0,128)    S^T (fp32), then P^T packed bf16 in its first 64 columns
-//   [128,256)  dP^T (fp32); once read, reused for the dQ_i tile
+// bwd_main warp roles (448 threads):
+//   warps 0-3, 4-7  compute for query half h = warp / 4 (64 queries of the
+//                   tile): P^T_h, dS^T_h, one thread per key row; dV (h = 0)
+//                   and dK (h = 1) epilogue
+//   warps 8-11      dQ writer: tensor memory -> shared memory -> TMA
+//                   reduce-add into the fp32 accumulator
+//   warp 12         TMA producer: K_j, V_j once; Q_i, dO_i, LSE2_i, D_i per step
+//   warp 13         MMA issuer
+// Tensor memory (lane = key row for S^T, dP^T, dV, dK):
+//   region h = [128 h, 128 h + 128): S^T_h at +0 (then P^T_h packed bf16),
+//              dP^T_h at +64 (once read, reused for the dQ product of half h)
 //   [256,256+D)      dV accumulator
 //   [256+D,256+2D)   dK accumulator
+// d = 128: the dQ product of half h is dQ^T_h = K^T dS^T_h (lane = feature,
+// column = query), issued right after dV/dK of half h, and staged in the rows
+// of the stage's Q and dO buffers that only half h's products read, so that
+// half 0's reduction overlaps half 1's compute.  d = 64: dQ_i = dS K once per
+// step (lane = query row).
 // Shared memory: K, V, two stages of (Q, dO, LSE2, D), and dS^T (bf16,
 // 128-byte swizzle), which serves as the K-major A operand of dK and, read
-// MN-major, as the A operand dS of dQ.
+// MN-major, as an operand of the dQ product.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -372,10 +380,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             mma_ss<false>(tDK, kmaj(sDS + h * T::BLK_BYTES, kk),
                                           mnmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_DVK,
                                           (t > 0 || h > 0 || kk > 0));
-                    }
-                    // dQ_i = dS K, in parts of 64 columns, each into the dP^T columns of region p
+                        if constexpr (D == 128) {
+                            // dQ^T for the 64 queries of half h = K^T dS^T_h (M = d, N = 64,
+                            // K = keys), into the dP^T columns of region h, issued as soon as
+                            // dS^T_h exists rather than after both halves
 #pragma unroll
-                    for (int p = 0; p < T::NDQ; ++p) {
+                            for (int kk = 0; kk < kTile / 16; ++kk)
+                                mma_ss<false>(tR + T::COL_DP, mnmaj(sK, kk), mnmaj(sDS + h * T::BLK_BYTES, kk),
+                                              T::IDESC_DQ, kk > 0);
+                            mma_commit(b_dq_full + 8u * h);
+                        }
+                    }
+                    // d = 64: dQ_i = dS K (M = queries, N = d) into the dP^T columns of region 0
+#pragma unroll
+                    for (int p = 0; p < (D == 128 ? 0 : T::NDQ); ++p) {
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
                             mma_ss<false>(tmem + p * T::COL_REGION + T::COL_DP, mnmaj(sDS, kk),
@@ -520,76 +538,147 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         constexpr int SLOTS_PER_BUF = T::TILE_BYTES / (kTile * 128);  // 16 KB boxes per buffer
         bool ok = true;
         int tt = 0, bh = q_bh0;
-        for (int t = 0; t < n_steps && ok; ++t, ++tt) {
-            if (tt == n_qh) {
-                tt = 0;
-                ++bh;
-            }
-            const int s = t % T::STAGES;
-            const int i = q_tile(tt);
-#pragma unroll
-            for (int p = 0; p < T::NDQ; ++p) {
-                if (!wait_warp(b_dq_full + 8u * p, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
-                    ok = false;
-                    break;
+        if constexpr (D == 128) {
+            // dQ^T_h sits in tensor memory with lane = feature, column = query: warp
+            // quarter wq holds features 32 wq .. +31, which is exactly one [64 x 32]
+            // fp32 box of the accumulator.  Half h is staged in the rows of the stage's
+            // Q and dO buffers that only half h's products read (done once dQ^T_h is).
+            for (int t = 0; t < n_steps && ok; ++t, ++tt) {
+                if (tt == n_qh) {
+                    tt = 0;
+                    ++bh;
                 }
-                tc_fence_after();
-                const uint32_t tq = tmem + p * T::COL_REGION + T::COL_DP + lane_off;
-                uint32_t v0[32], v1[32];
-                tmem_ld32(tq, v0);
-                tmem_ld32(tq + 32, v1);
-                tmem_ld_wait(v0);
-                tmem_ld_wait(v1);
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_dq_empty + 8u * p);  // part p has left tensor memory
+                const int s = t % T::STAGES;
+                const int i = q_tile(tt);
+                auto box_addr = [&](int b, int h) {
+                    return (b < 2 ? T::OFF_Q + b * T::BLK_BYTES : T::OFF_DO + (b - 2) * T::BLK_BYTES) +
+                           s * T::TILE_BYTES + h * T::HALF_BYTES;
+                };
 #pragma unroll
-                for (int b = 0; b < 2; ++b) {
-                    const int u = 2 * p + b;  // staging box
-                    const uint32_t box = sbase +
-                                         (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
-                                                            : T::OFF_DO + s * T::TILE_BYTES +
-                                                                  (u - SLOTS_PER_BUF) * 16384);
-                    uint8_t* row = smem + (box - sbase) + r * 128;
-                    const uint32_t(&v)[32] = b ? v1 : v0;
-#pragma unroll
-                    for (int x = 0; x < 8; ++x)
-                        *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) << 4)) =
-                            make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(b_dq_staged + 8u * p);
-                if (warp == 8) {
-                    // Every writer warp has staged its rows.  A bounded wait, never a bare
-                    // bar.sync: a warp that gave up must not strand the others.  The
-                    // outcome is made uniform across warp 8 before anyone acts on it.
-                    bool staged = true;
-                    if (lane == 0)
-                        staged = wait_one(b_dq_staged + 8u * p, t & 1, abort_flag, prm.st,
-                                          SITE_DQ_STAGED);
-                    if (!__shfl_sync(0xffffffffu, staged ? 1 : 0, 0)) {
+                for (int h = 0; h < 2; ++h) {
+                    if (!wait_warp(b_dq_full + 8u * h, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
                         ok = false;
                         break;
                     }
-                }
-                if (leader) {
+                    tc_fence_after();
+                    const uint32_t tq = tmem + h * T::COL_REGION + T::COL_DP + lane_off;
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tq, v0);
+                    tmem_ld32(tq + 32, v1);
+                    tmem_ld_wait(v0);
+                    tmem_ld_wait(v1);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_dq_empty + 8u * h);  // dQ^T_h has left tensor memory
+                    // row q of the box: 128 bytes, 16-byte chunk (lane / 4) ^ (q % 8)
+                    uint8_t* box = smem + box_addr(wq, h) + (lane & 3) * 4;
+                    const int c16 = lane >> 2;
 #pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        *reinterpret_cast<uint32_t*>(box + q * 128 + ((c16 ^ (q & 7)) << 4)) = v0[q];
+#pragma unroll
+                    for (int q = 0; q < 32; ++q)
+                        *reinterpret_cast<uint32_t*>(box + (32 + q) * 128 + ((c16 ^ (q & 7)) << 4)) = v1[q];
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_dq_staged + 8u * h);
+                    if (warp == 8) {
+                        // Every writer warp has staged its box.  A bounded wait, never a
+                        // bare bar.sync; the outcome is made uniform across warp 8.
+                        bool staged = true;
+                        if (lane == 0)
+                            staged = wait_one(b_dq_staged + 8u * h, t & 1, abort_flag, prm.st,
+                                              SITE_DQ_STAGED);
+                        if (!__shfl_sync(0xffffffffu, staged ? 1 : 0, 0)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (leader) {
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            tma_reduce_add_3d(&tm_dq, sbase + box_addr(b, h), 32 * b, i * kTile + 64 * h, bh);
+                        bulk_commit_group();
+                    }
+                }
+                if (!ok) break;
+                if (leader) {
+                    bulk_wait_group_read0();       // the stage's bytes have been read
+                    mbar_arrive(b_qdo_empty(s));   // second arrival: the producer may refill it
+                }
+            }
+        } else {
+            for (int t = 0; t < n_steps && ok; ++t, ++tt) {
+                if (tt == n_qh) {
+                    tt = 0;
+                    ++bh;
+                }
+                const int s = t % T::STAGES;
+                const int i = q_tile(tt);
+    #pragma unroll
+                for (int p = 0; p < T::NDQ; ++p) {
+                    if (!wait_warp(b_dq_full + 8u * p, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tq = tmem + p * T::COL_REGION + T::COL_DP + lane_off;
+                    uint32_t v0[32], v1[32];
+                    tmem_ld32(tq, v0);
+                    tmem_ld32(tq + 32, v1);
+                    tmem_ld_wait(v0);
+                    tmem_ld_wait(v1);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_dq_empty + 8u * p);  // part p has left tensor memory
+    #pragma unroll
                     for (int b = 0; b < 2; ++b) {
-                        const int u = 2 * p + b;
+                        const int u = 2 * p + b;  // staging box
                         const uint32_t box = sbase +
                                              (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
                                                                 : T::OFF_DO + s * T::TILE_BYTES +
                                                                       (u - SLOTS_PER_BUF) * 16384);
-                        tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
+                        uint8_t* row = smem + (box - sbase) + r * 128;
+                        const uint32_t(&v)[32] = b ? v1 : v0;
+    #pragma unroll
+                        for (int x = 0; x < 8; ++x)
+                            *reinterpret_cast<uint4*>(row + ((x ^ (r & 7)) << 4)) =
+                                make_uint4(v[4 * x], v[4 * x + 1], v[4 * x + 2], v[4 * x + 3]);
                     }
-                    bulk_commit_group();
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(b_dq_staged + 8u * p);
+                    if (warp == 8) {
+                        // Every writer warp has staged its rows.  A bounded wait, never a bare
+                        // bar.sync: a warp that gave up must not strand the others.  The
+                        // outcome is made uniform across warp 8 before anyone acts on it.
+                        bool staged = true;
+                        if (lane == 0)
+                            staged = wait_one(b_dq_staged + 8u * p, t & 1, abort_flag, prm.st,
+                                              SITE_DQ_STAGED);
+                        if (!__shfl_sync(0xffffffffu, staged ? 1 : 0, 0)) {
+                            ok = false;
+                            break;
+                        }
+                    }
+                    if (leader) {
+    #pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            const int u = 2 * p + b;
+                            const uint32_t box = sbase +
+                                                 (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
+                                                                    : T::OFF_DO + s * T::TILE_BYTES +
+                                                                          (u - SLOTS_PER_BUF) * 16384);
+                            tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
+                        }
+                        bulk_commit_group();
+                    }
                 }
-            }
-            if (!ok) break;
-            if (leader) {
-                bulk_wait_group_read0();       // the stage's bytes have been read
-                mbar_arrive(b_qdo_empty(s));   // second arrival: the producer may refill it
+                if (!ok) break;
+                if (leader) {
+                    bulk_wait_group_read0();       // the stage's bytes have been read
+                    mbar_arrive(b_qdo_empty(s));   // second arrival: the producer may refill it
+                }
             }
         }
         if (leader) bulk_wait_group0();  // every reduction has landed before the CTA retires
