@@ -252,7 +252,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(b_kv, 1);
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(b_qdo_full(s), 1);
-            mbar_init(b_qdo_empty(s), 2);  // MMA commit + dQ writer (its reductions read the stage)
+            // MMA commit, and for d = 64 the dQ writer (its reductions read the stage)
+            mbar_init(b_qdo_empty(s), D == 128 ? 1 : 2);
         }
         for (int h = 0; h < 2; ++h) {
             mbar_init(b_s_full + 8u * h, 1);
@@ -329,11 +330,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint32_t sK = sbase + T::OFF_K, sV = sbase + T::OFF_V, sDS = sbase + T::OFF_DS;
             // K-major operand, 16 bf16 (32 bytes) of K per instruction.
             auto kmaj = [](uint32_t base, int kk) {
-                return sw128_desc(base + (kk >> 2) * T::BLK_BYTES + (kk & 3) * 32, 16, 1024);
+                return desc_add(sw128_desc_words(base, 16, 1024), (kk >> 2) * T::BLK_BYTES + (kk & 3) * 32);
             };
             // MN-major operand: rows are the reduction index, 16 rows per instruction.
             auto mnmaj = [](uint32_t base, int kk) {
-                return sw128_desc(base + kk * 16 * 128, T::BLK_BYTES, 1024);
+                return desc_add(sw128_desc_words(base, T::BLK_BYTES, 1024), kk * 16 * 128);
             };
             auto run = [&]() -> bool {
                 if (!wait_one(b_kv, 0, abort_flag, prm.st, SITE_KV)) return false;
@@ -349,7 +350,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         // S^T_h = K Q_h^T  (M = 128 keys, N = 64 queries, K = d)
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss<false>(tR, kmaj(sK, kk), kmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_SDP,
+                            mma_ss_bf16(tR, kmaj(sK, kk), kmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_SDP,
                                           kk > 0);
                         if (t > 0 && h < T::NDQ) {  // dQ part h of the previous tile has left
                             if (!wait_one(b_dq_empty + 8u * h, (t - 1) & 1, abort_flag, prm.st,
@@ -360,7 +361,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         // dP^T_h = V dO_h^T
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss<false>(tR + T::COL_DP, kmaj(sV, kk), kmaj(sDO + h * T::HALF_BYTES, kk),
+                            mma_ss_bf16(tR + T::COL_DP, kmaj(sV, kk), kmaj(sDO + h * T::HALF_BYTES, kk),
                                           T::IDESC_SDP, kk > 0);
                         mma_commit(b_s_full + 8u * h);
                     }
@@ -372,12 +373,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         // dV += P^T_h dO_h : A = P^T_h (tensor memory), B = dO_h (MN-major)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ts<false>(tDV, tR + kk * 8, mnmaj(sDO + h * T::HALF_BYTES, kk),
+                            mma_ts_bf16(tDV, tR + kk * 8, mnmaj(sDO + h * T::HALF_BYTES, kk),
                                           T::IDESC_DVK, (t > 0 || h > 0 || kk > 0));
                         // dK += dS^T_h Q_h : A = dS^T block h (K-major), B = Q_h (MN-major)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_ss<false>(tDK, kmaj(sDS + h * T::BLK_BYTES, kk),
+                            mma_ss_bf16(tDK, kmaj(sDS + h * T::BLK_BYTES, kk),
                                           mnmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_DVK,
                                           (t > 0 || h > 0 || kk > 0));
                         if constexpr (D == 128) {
@@ -386,7 +387,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                             // dS^T_h exists rather than after both halves
 #pragma unroll
                             for (int kk = 0; kk < kTile / 16; ++kk)
-                                mma_ss<false>(tR + T::COL_DP, mnmaj(sK, kk), mnmaj(sDS + h * T::BLK_BYTES, kk),
+                                mma_ss_bf16(tR + T::COL_DP, mnmaj(sK, kk), mnmaj(sDS + h * T::BLK_BYTES, kk),
                                               T::IDESC_DQ, kk > 0);
                             mma_commit(b_dq_full + 8u * h);
                         }
@@ -396,7 +397,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     for (int p = 0; p < (D == 128 ? 0 : T::NDQ); ++p) {
 #pragma unroll
                         for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss<false>(tmem + p * T::COL_REGION + T::COL_DP, mnmaj(sDS, kk),
+                            mma_ss_bf16(tmem + p * T::COL_REGION + T::COL_DP, mnmaj(sDS, kk),
                                           mnmaj(sK + p * T::BLK_BYTES, kk), T::IDESC_DQ, kk > 0);
                         mma_commit(b_dq_full + 8u * p);
                     }
@@ -539,21 +540,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         bool ok = true;
         int tt = 0, bh = q_bh0;
         if constexpr (D == 128) {
-            // dQ^T_h sits in tensor memory with lane = feature, column = query: warp
-            // quarter wq holds features 32 wq .. +31, which is exactly one [64 x 32]
-            // fp32 box of the accumulator.  Half h is staged in the rows of the stage's
-            // Q and dO buffers that only half h's products read (done once dQ^T_h is).
+            // dQ^T_h sits in tensor memory with lane = feature, column = query, so one
+            // warp-wide fp32 reduction covers 32 consecutive features of one query row:
+            // a whole 128-byte line of the accumulator.  The adds go straight from
+            // registers to L2; nothing is staged, and the Q/dO stage is handed back by
+            // the MMA issuer alone as soon as the tile's products have read it.
+            float* acc_col = prm.dq_acc + static_cast<size_t>(wq * 32 + lane);
             for (int t = 0; t < n_steps && ok; ++t, ++tt) {
                 if (tt == n_qh) {
                     tt = 0;
                     ++bh;
                 }
-                const int s = t % T::STAGES;
                 const int i = q_tile(tt);
-                auto box_addr = [&](int b, int h) {
-                    return (b < 2 ? T::OFF_Q + b * T::BLK_BYTES : T::OFF_DO + (b - 2) * T::BLK_BYTES) +
-                           s * T::TILE_BYTES + h * T::HALF_BYTES;
-                };
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     if (!wait_warp(b_dq_full + 8u * h, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
@@ -570,41 +568,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(b_dq_empty + 8u * h);  // dQ^T_h has left tensor memory
-                    // row q of the box: 128 bytes, 16-byte chunk (lane / 4) ^ (q % 8)
-                    uint8_t* box = smem + box_addr(wq, h) + (lane & 3) * 4;
-                    const int c16 = lane >> 2;
+                    float* row0 = acc_col + (static_cast<size_t>(bh) * prm.Npad + i * kTile + 64 * h) * D;
 #pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        *reinterpret_cast<uint32_t*>(box + q * 128 + ((c16 ^ (q & 7)) << 4)) = v0[q];
+                    for (int q = 0; q < 32; ++q) red_add_f32(row0 + q * D, __uint_as_float(v0[q]));
 #pragma unroll
-                    for (int q = 0; q < 32; ++q)
-                        *reinterpret_cast<uint32_t*>(box + (32 + q) * 128 + ((c16 ^ (q & 7)) << 4)) = v1[q];
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(b_dq_staged + 8u * h);
-                    if (warp == 8) {
-                        // Every writer warp has staged its box.  A bounded wait, never a
-                        // bare bar.sync; the outcome is made uniform across warp 8.
-                        bool staged = true;
-                        if (lane == 0)
-                            staged = wait_one(b_dq_staged + 8u * h, t & 1, abort_flag, prm.st,
-                                              SITE_DQ_STAGED);
-                        if (!__shfl_sync(0xffffffffu, staged ? 1 : 0, 0)) {
-                            ok = false;
-                            break;
-                        }
-                    }
-                    if (leader) {
-#pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            tma_reduce_add_3d(&tm_dq, sbase + box_addr(b, h), 32 * b, i * kTile + 64 * h, bh);
-                        bulk_commit_group();
-                    }
-                }
-                if (!ok) break;
-                if (leader) {
-                    bulk_wait_group_read0();       // the stage's bytes have been read
-                    mbar_arrive(b_qdo_empty(s));   // second arrival: the producer may refill it
+                    for (int q = 0; q < 32; ++q) red_add_f32(row0 + (32 + q) * D, __uint_as_float(v1[q]));
                 }
             }
         } else {

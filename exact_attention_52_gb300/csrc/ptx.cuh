@@ -376,6 +376,42 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
         : "memory");
 }
 
+// A shared-memory descriptor kept as its two 32-bit words.  The start address
+// sits in the low word (bits 0-13, address >> 4), so a byte offset b is added
+// as lo + (b >> 4): shared memory is below 256 KB, so the field never carries.
+struct SmemDesc {
+    uint32_t lo, hi;
+};
+
+__device__ __forceinline__ SmemDesc sw128_desc_words(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    const uint64_t d = sw128_desc(saddr, lbo, sbo);
+    return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
+__device__ __forceinline__ SmemDesc desc_add(SmemDesc d, uint32_t byte_offset) {
+    return SmemDesc{d.lo + (byte_offset >> 4), d.hi};
+}
+
+// bf16 products with the descriptors passed as words (fewer instructions per
+// issue than building the 64-bit descriptor each time).
+__device__ __forceinline__ void mma_ss_bf16(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
+        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
+        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // Warp-wide forms: every lane of a converged warp executes the call with the
 // same (warp-uniform) operands and one lane, chosen by elect.sync, issues the
 // instruction.  Keeping the issuing loop on the whole warp lets the compiler
@@ -501,6 +537,10 @@ __device__ __forceinline__ float add_bf16x2(float acc, uint32_t w) {
         : "+f"(acc)
         : "r"(w));
     return acc;
+}
+
+__device__ __forceinline__ void red_add_f32(float* gaddr, float a) {
+    asm volatile("red.global.add.f32 [%0], %1;" ::"l"(gaddr), "f"(a) : "memory");
 }
 
 __device__ __forceinline__ void red_add_v4(float* gaddr, float a, float b, float c, float d) {
