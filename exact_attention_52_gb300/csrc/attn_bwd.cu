@@ -20,8 +20,9 @@
 //   warps 0-3, 4-7  compute for query half h = warp / 4 (64 queries of the
 //                   tile): P^T_h, dS^T_h, one thread per key row; dV (h = 0)
 //                   and dK (h = 1) epilogue
-//   warps 8-11      dQ writer: tensor memory -> shared memory -> TMA
-//                   reduce-add into the fp32 accumulator
+//   warps 8-11      dQ writer: tensor memory -> fp32 reductions into the
+//                   accumulator (d = 128: straight from registers; d = 64:
+//                   staged in shared memory, TMA reduce-add)
 //   warp 12         TMA producer: K_j, V_j once; Q_i, dO_i, LSE2_i, D_i per step
 //   warp 13         MMA issuer
 // Tensor memory (lane = key row for S^T, dP^T, dV, dK):
@@ -30,10 +31,10 @@
 //   [256,256+D)      dV accumulator
 //   [256+D,256+2D)   dK accumulator
 // d = 128: the dQ product of half h is dQ^T_h = K^T dS^T_h (lane = feature,
-// column = query), issued right after dV/dK of half h, and staged in the rows
-// of the stage's Q and dO buffers that only half h's products read, so that
-// half 0's reduction overlaps half 1's compute.  d = 64: dQ_i = dS K once per
-// step (lane = query row).
+// column = query), issued right after dV/dK of half h, so that half 0's
+// reduction overlaps half 1's compute; a warp's red.global.add.f32 then covers
+// one 128-byte line of the accumulator.  d = 64: dQ_i = dS K once per step
+// (lane = query row), staged and TMA-reduced.
 // Shared memory: K, V, two stages of (Q, dO, LSE2, D), and dS^T (bf16,
 // 128-byte swizzle), which serves as the K-major A operand of dK and, read
 // MN-major, as an operand of the dQ product.
