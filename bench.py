@@ -452,6 +452,11 @@ EXTRA_WORKLOADS = {
                                          window=(1024, 0)),
     # one head, long sequence (64 CTAs without splitting): key tiles split across CTAs
     "splitkv_b1_h1_n16384_d128": dict(B=1, H=1, Hk=1, N=16384, d=128, causal=False, splitkv=True),
+    # the small configurations of the parity suite: one CTA (latency), a d = 64 case
+    # near the ridge point, and causal d = 128 forward + backward
+    "c1_fwd_b1_h1_n128_d64": dict(B=1, H=1, Hk=1, N=128, d=64, causal=False, fwd_only=True),
+    "c2_fwd_b4_h16_n1024_d64": dict(B=4, H=16, Hk=16, N=1024, d=64, causal=False, fwd_only=True),
+    "c3_causal_b2_h16_n4096_d128": dict(B=2, H=16, Hk=16, N=4096, d=128, causal=True),
 }
 
 
@@ -504,7 +509,9 @@ def run_extra(args):
             api.fwd(q, k, v, causal=causal, o=o, lse=lse)
         if ev:
             ev[1].record(stream)
-        if window is not None:
+        if w.get("fwd_only"):
+            pass
+        elif window is not None:
             api.bwd_window(q, k, v, o, do, lse, *window, dq=dq, dk=dk, dv=dv, workspace=ws)
         elif w.get("splitkv"):
             api.fwd(q, k, v, causal=causal, o=o, lse=lse)  # single-pass forward, for comparison
@@ -531,6 +538,19 @@ def run_extra(args):
         f = B * H * window_flops(N, D, *window)
     peaks, kind = load_peaks()
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    if w.get("fwd_only"):
+        nbytes = attn_bytes(B, H, N, D, "fwd")
+        line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
+                "unit": "TFLOP/s", "value": round(f / (fwd_ms * 1e-3) / 1e12, 3),
+                "components": {"fwd": {"us": round(fwd_ms * 1e3, 2),
+                                       "tflops": round(f / (fwd_ms * 1e-3) / 1e12, 3),
+                                       "gbs": round(nbytes / (fwd_ms * 1e-3) / 1e9, 1),
+                                       "frac_of_burst": round(f / (fwd_ms * 1e-3) / 1e12 / burst, 4)}},
+                "note": "time per call between CUDA events, host-side argument checks and "
+                        "tensor-map encoding included",
+                "peak_kind": kind, "dtype": "bf16", "data": "synthetic"}
+        print(json.dumps(line), flush=True)
+        return 0
     if w.get("splitkv"):
         line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
                 "unit": "TFLOP/s", "value": round(f / (fwd_ms * 1e-3) / 1e12, 2),
