@@ -44,6 +44,7 @@ FP8 = dict(B=1, H=16, N=16384, d=128, causal=True)
 WORKLOAD = ("fwd+bwd bf16 B1 H32 N8192 d128 (1% keys x8) + fp8 fwd B1 H16 N16384 d128 causal")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+CPU_BASELINE_S = 10.0  # host seconds spent on the oracle sample of the default run
 REF_BUDGET_S = 90.0  # wall time of the whole --impl reference run
 
 
@@ -292,12 +293,16 @@ def run_ours(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         data = oracle_sample_data()
-        n_rows = BF16["N"]  # the whole of head 0: about 10-30 s of host work
+        n_rows = BF16["N"]  # the whole of head 0 per pass
+        # Passes over that sample until about 10 s of host work (at most 8 passes).
         t0 = time.perf_counter()
-        f = oracle_sample_step(data, n_rows)
+        f, passes = 0.0, 0
+        while passes < 8 and (passes == 0 or time.perf_counter() - t0 < CPU_BASELINE_S):
+            f += oracle_sample_step(data, n_rows)
+            passes += 1
         dt = time.perf_counter() - t0
         cpu = {"value": f / dt / 1e12, "unit": "TFLOP/s", "cores": cpu_cores(), "kind": "oracle",
-               "sample": sample_desc(n_rows) + f" (one pass, {dt:.1f} s)"}
+               "sample": sample_desc(n_rows) + f" ({passes} passes, {dt:.1f} s)"}
         del data
 
     host, d = make_device_data(torch, dev)
