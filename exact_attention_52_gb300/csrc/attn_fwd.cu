@@ -4,8 +4,9 @@
 // 1-2; FlashAttention paper item 58: running max, running sum, and the same
 // rescale applied to the output accumulator).
 //
-// One CTA owns two 128-row query tiles of one (batch, head) and streams the
-// key/value tiles of that head through a shared-memory ring:
+// A work item is two 128-row query tiles of one (batch, head); a CTA streams the
+// item's key/value tiles through a shared-memory ring (persistent CTAs loop over
+// items, see the work assignment below):
 //
 //   warp 8      TMA producer: Q tiles once, then K_j, V_j into the ring
 //   warp 9      MMA issuer (one thread): S_g = Q_g K_j^T and O_g += P_g V_j on
@@ -52,8 +53,9 @@ struct FwdTraits {
     static constexpr int KV_SLOTS = TILE_BYTES == 32768 ? 5 : 8;
     static constexpr int SMEM_Q = 2 * TILE_BYTES;
     static constexpr int SMEM_KV = KV_SLOTS * TILE_BYTES;
-    // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done
-    static constexpr int NBARS = 1 + 2 * KV_SLOTS + 2 + 2 + 2 + 1;
+    // barriers: q_full, kv_full[S], kv_empty[S], s_full[2], p_full[2], o_full[2], mma_done,
+    //           q_empty
+    static constexpr int NBARS = 1 + 2 * KV_SLOTS + 2 + 2 + 2 + 1 + 1;
     static constexpr int SMEM_BYTES = SMEM_Q + SMEM_KV + NBARS * 8 + 16;
     static constexpr uint32_t COL_S0 = 0, COL_S1 = 128, COL_O0 = 256, COL_O1 = 256 + D;
     static constexpr uint32_t FMT = FP8 ? kFmtE4M3 : kFmtBF16;
@@ -67,7 +69,7 @@ struct FwdTraits {
 // Site ids recorded when a wait gives up (kernel 1 = forward).
 enum : uint32_t {
     SITE_Q = 0x101, SITE_KV_EMPTY = 0x102, SITE_KV_FULL = 0x103, SITE_P_FULL = 0x104,
-    SITE_S_FULL = 0x105, SITE_O_FULL = 0x106, SITE_DRAIN = 0x107,
+    SITE_S_FULL = 0x105, SITE_O_FULL = 0x106, SITE_DRAIN = 0x107, SITE_Q_EMPTY = 0x108,
 };
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
@@ -97,6 +99,7 @@ __global__ void __launch_bounds__(320, 1)
     const uint32_t b_p_full = b_s_full + 16u;                        // +8*g
     const uint32_t b_o_full = b_p_full + 16u;                        // +8*g
     const uint32_t b_done = b_o_full + 16u;
+    const uint32_t b_q_empty = b_done + 8u;  // every product reading the Q tiles of an item is done
 
     if ((smem_u32(smem) & 1023u) != 0) {  // swizzle atoms need 1024-byte alignment
         if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x1FF);
@@ -104,46 +107,62 @@ __global__ void __launch_bounds__(320, 1)
     }
 
     // ---- work assignment ----
-    // Without a mask (and for sliding windows) head-major order, so the CTAs
-    // resident at any time cover only a few heads and each head's K and V come
-    // from HBM about once.  Causal: heaviest query tiles of every head first
-    // (longest-first keeps the tail of the launch short).
-    // Split-KV: the splits of one query-tile pair are adjacent CTAs.
-    const unsigned cta = blockIdx.x / prm.n_splits;
-    const int split = static_cast<int>(blockIdx.x % prm.n_splits);
+    // The CTAs are persistent: CTA c takes work items c, c + G, c + 2G, ... (G =
+    // gridDim.x), so that setting up barriers and tensor memory happens once and one
+    // item's epilogue overlaps the next item's loads and first products.  An item is
+    // a query-tile pair of one (batch, head) and, for split-KV, one split.
+    // Without a mask (and for sliding windows) items are numbered head-major, so the
+    // items in flight cover only a few heads and each head's K and V come from HBM
+    // about once.  Causal: heaviest query tiles of every head first (longest-first
+    // keeps the tail short).  Split-KV: the splits of one pair are adjacent items.
     const bool split_mode = prm.n_splits > 1;
     const bool lpt = prm.causal != 0;
-    const int bh = lpt ? static_cast<int>(cta % prm.BH) : static_cast<int>(cta / prm.n_pairs);
-    const int pair = prm.n_pairs - 1 -
-                     (lpt ? static_cast<int>(cta / prm.BH) : static_cast<int>(cta % prm.n_pairs));
     const int N = prm.N;
-    const int n_kv_total = (N + kTile - 1) / kTile;
-    // Query tile g of this CTA uses key tiles [lo_t[g], lo_t[g] + n_t[g]): the
-    // tiles holding keys visible to some row of the tile (window
-    // i - win_left <= key <= i + win_right, a negative bound meaning none),
-    // cut to this CTA's split.
-    int lo_t[2], n_t[2];
+    const int n_items = prm.BH * prm.n_pairs * prm.n_splits;
+    struct Item {
+        int split, bh, pair, kv_lo, n_kv, b_idx, h_idx, hk_idx;
+        int lo0, lo1, n0, n1;  // key-tile range [lo_g, lo_g + n_g) of query tile g
+        __device__ int lo(int g) const { return g ? lo1 : lo0; }
+        __device__ int n(int g) const { return g ? n1 : n0; }
+    };
+    auto item_info = [&](int item) {
+        Item w;
+        const int cta = item / prm.n_splits;
+        w.split = item % prm.n_splits;
+        w.bh = lpt ? cta % prm.BH : cta / prm.n_pairs;
+        w.pair = prm.n_pairs - 1 - (lpt ? cta / prm.BH : cta % prm.n_pairs);
+        // Query tile g uses key tiles [lo_g, lo_g + n_g): the tiles holding
+        // keys visible to some row of the tile (window i - win_left <= key <=
+        // i + win_right, a negative bound meaning none), cut to the item's split.
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        const int qt = 2 * pair + g;
-        const int r0 = qt * kTile, r1 = min(N - 1, qt * kTile + kTile - 1);
-        const int key_lo = prm.win_left < 0 ? 0 : max(0, r0 - prm.win_left);
-        const int key_hi = prm.win_right < 0 ? N - 1 : min(N - 1, r1 + prm.win_right);
-        const int lo = max(key_lo / kTile, split * prm.split_len);
-        const int hi = min(key_hi / kTile, split * prm.split_len + prm.split_len - 1);
-        const bool live = r0 < N && key_lo <= key_hi && hi >= lo;
-        lo_t[g] = live ? lo : 0;
-        n_t[g] = live ? hi - lo + 1 : 0;
-    }
-    // The CTA streams key tiles [kv_lo, kv_lo + n_kv): the union of both ranges
-    // (they overlap or touch: the two tiles' rows are adjacent).
-    const int kv_lo = n_t[0] > 0 ? (n_t[1] > 0 ? min(lo_t[0], lo_t[1]) : lo_t[0]) : lo_t[1];
-    const int kv_hi = max(n_t[0] > 0 ? lo_t[0] + n_t[0] : 0, n_t[1] > 0 ? lo_t[1] + n_t[1] : 0);
-    const int n_kv = (n_t[0] > 0 || n_t[1] > 0) ? kv_hi - kv_lo : 0;
-    // Key/value head of this query head (grouped-query attention: H/Hk query
-    // heads share one key/value head; Hk == H is ordinary multi-head attention).
-    const int b_idx = bh / prm.H, h_idx = bh % prm.H;  // batch and query head
-    const int hk_idx = h_idx / (prm.H / prm.Hk);          // key/value head
+        for (int g = 0; g < 2; ++g) {
+            const int qt = 2 * w.pair + g;
+            const int r0 = qt * kTile, r1 = min(N - 1, qt * kTile + kTile - 1);
+            const int key_lo = prm.win_left < 0 ? 0 : max(0, r0 - prm.win_left);
+            const int key_hi = prm.win_right < 0 ? N - 1 : min(N - 1, r1 + prm.win_right);
+            const int lo = max(key_lo / kTile, w.split * prm.split_len);
+            const int hi = min(key_hi / kTile, w.split * prm.split_len + prm.split_len - 1);
+            const bool live = r0 < N && key_lo <= key_hi && hi >= lo;
+            if (g == 0) {
+                w.lo0 = live ? lo : 0;
+                w.n0 = live ? hi - lo + 1 : 0;
+            } else {
+                w.lo1 = live ? lo : 0;
+                w.n1 = live ? hi - lo + 1 : 0;
+            }
+        }
+        // The item streams key tiles [kv_lo, kv_lo + n_kv): the union of both ranges
+        // (they overlap or touch: the two tiles' rows are adjacent).
+        w.kv_lo = w.n(0) > 0 ? (w.n(1) > 0 ? min(w.lo(0), w.lo(1)) : w.lo(0)) : w.lo(1);
+        const int kv_hi = max(w.n(0) > 0 ? w.lo(0) + w.n(0) : 0, w.n(1) > 0 ? w.lo(1) + w.n(1) : 0);
+        w.n_kv = (w.n(0) > 0 || w.n(1) > 0) ? kv_hi - w.kv_lo : 0;
+        // Key/value head of the query head (grouped-query attention: H/Hk query heads
+        // share one key/value head; Hk == H is ordinary multi-head attention).
+        w.b_idx = w.bh / prm.H;
+        w.h_idx = w.bh % prm.H;
+        w.hk_idx = w.h_idx / (prm.H / prm.Hk);
+        return w;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
@@ -157,6 +176,7 @@ __global__ void __launch_bounds__(320, 1)
             mbar_init(b_o_full + 8u * g, 1);
         }
         mbar_init(b_done, 1);
+        mbar_init(b_q_empty, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -177,36 +197,45 @@ __global__ void __launch_bounds__(320, 1)
     if (warp == 8) {
         // ================= TMA producer =================
         if (lane == 0) {
-            const int q_tiles = (n_t[0] > 0) + (n_t[1] > 0);
-            mbar_arrive_expect_tx(b_q, q_tiles * T::TILE_BYTES);
-            for (int g = 0; g < 2; ++g) {
-                if (n_t[g] == 0) continue;
-                for (int blk = 0; blk < T::NBLK; ++blk)
-                    tma_load_4d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
-                                blk * T::BLK_ELEMS, (2 * pair + g) * kTile, h_idx, b_idx);
-            }
-            int idx = 0;
+            int idx = 0;  // K/V loads issued so far (ring position), over all items
+            int k = 0;    // items started
             bool ok = true;
-            for (int j = 0; j < n_kv && ok; ++j) {
-                for (int t = 0; t < 2; ++t, ++idx) {  // t = 0: K_j, t = 1: V_j
-                    const int slot = idx % T::KV_SLOTS;
-                    const int round = idx / T::KV_SLOTS;
-                    if (round > 0 &&
-                        !wait_one(b_kv_empty(slot), (round - 1) & 1, abort_flag, prm.st,
-                                  SITE_KV_EMPTY)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_expect_tx(b_kv_full(slot), T::TILE_BYTES);
-                    const CUtensorMap* map = t ? &tm_v : &tm_k;
+            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++k) {
+                const Item it = item_info(item);
+                // The previous item's products that read Q have completed.
+                if (k > 0 && !wait_one(b_q_empty, (k - 1) & 1, abort_flag, prm.st, SITE_Q_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const int q_tiles = (it.n(0) > 0) + (it.n(1) > 0);
+                mbar_arrive_expect_tx(b_q, q_tiles * T::TILE_BYTES);
+                for (int g = 0; g < 2; ++g) {
+                    if (it.n(g) == 0) continue;
                     for (int blk = 0; blk < T::NBLK; ++blk)
-                        tma_load_4d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
-                                    b_kv_full(slot), blk * T::BLK_ELEMS, (kv_lo + j) * kTile, hk_idx,
-                                    b_idx);
+                        tma_load_4d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
+                                    blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile, it.h_idx, it.b_idx);
+                }
+                for (int j = 0; j < it.n_kv && ok; ++j) {
+                    for (int t = 0; t < 2; ++t, ++idx) {  // t = 0: K_j, t = 1: V_j
+                        const int slot = idx % T::KV_SLOTS;
+                        const int round = idx / T::KV_SLOTS;
+                        if (round > 0 &&
+                            !wait_one(b_kv_empty(slot), (round - 1) & 1, abort_flag, prm.st,
+                                      SITE_KV_EMPTY)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_expect_tx(b_kv_full(slot), T::TILE_BYTES);
+                        const CUtensorMap* map = t ? &tm_v : &tm_k;
+                        for (int blk = 0; blk < T::NBLK; ++blk)
+                            tma_load_4d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
+                                        b_kv_full(slot), blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile,
+                                        it.hk_idx, it.b_idx);
+                    }
                 }
             }
             // Let every copy this thread started land before the CTA can exit.
-            wait_drain(b_q, 0, prm.st, SITE_DRAIN);
+            if (k > 0) wait_drain(b_q, (k - 1) & 1, prm.st, SITE_DRAIN);
             const int first = idx > T::KV_SLOTS ? idx - T::KV_SLOTS : 0;
             for (int i = first; i < idx; ++i)
                 wait_drain(b_kv_full(i % T::KV_SLOTS), (i / T::KV_SLOTS) & 1, prm.st, SITE_DRAIN);
@@ -219,6 +248,9 @@ __global__ void __launch_bounds__(320, 1)
         {
             const uint32_t sq_base = smem_u32(sQ);
             const uint32_t skv_base = smem_u32(sKV);
+            Item it{};        // the item being issued
+            int ring = 0;     // ring position of the item's first K tile (K/V loads before it)
+            int pdone0 = 0, pdone1 = 0;  // P tiles of query tile 0 / 1 consumed in earlier items
             auto slot_addr = [&](int idx) {
                 return skv_base + static_cast<uint32_t>((idx % T::KV_SLOTS) * T::TILE_BYTES);
             };
@@ -226,50 +258,58 @@ __global__ void __launch_bounds__(320, 1)
                 return wait_warp(b_kv_full(idx % T::KV_SLOTS), (idx / T::KV_SLOTS) & 1, abort_flag,
                                 prm.st, SITE_KV_FULL);
             };
+            // Ring index of K_j / V_j (j absolute), in the producer's load order.
+            auto kidx = [&](int j) { return ring + 2 * (j - it.kv_lo); };
             // S_g = Q_g K_j^T : both operands K-major, 32 bytes of K per instruction.
             auto issue_s = [&](int g, int j) {
                 const uint32_t qa = sq_base + g * T::TILE_BYTES;
-                const uint32_t kb = slot_addr(2 * (j - kv_lo));
+                const uint32_t kb = slot_addr(kidx(j));
 #pragma unroll
                 for (int kk = 0; kk < D / T::UMMA_K; ++kk) {
                     const uint32_t off = (kk * 32) / 128 * T::BLK_BYTES + (kk * 32) % 128;
-                    mma_ss_warp<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), sw128_desc(qa + off, 16, 1024), sw128_desc(kb + off, 16, 1024),
-                                T::IDESC_S, kk > 0 ? 1u : 0u);
+                    mma_ss_warp<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), sw128_desc(qa + off, 16, 1024),
+                                     sw128_desc(kb + off, 16, 1024), T::IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_warp(b_s_full + 8u * g);
             };
             // O_g += P_g V_j : P from tensor memory, V MN-major (rows = keys).
             auto issue_pv = [&](int g, int j, bool first) {
-                const uint32_t vb = slot_addr(2 * (j - kv_lo) + 1);
+                const uint32_t vb = slot_addr(kidx(j) + 1);
 #pragma unroll
                 for (int kk = 0; kk < kTile / T::UMMA_K; ++kk) {
                     mma_ts_warp<FP8>(tmem + (g ? T::COL_O1 : T::COL_O0),
-                                tmem + (g ? T::COL_S1 : T::COL_S0) + kk * 8,
-                                sw128_desc(vb + kk * T::UMMA_K * 128, T::BLK_BYTES, 1024), T::IDESC_PV,
-                                (!first || kk > 0) ? 1u : 0u);
+                                     tmem + (g ? T::COL_S1 : T::COL_S0) + kk * 8,
+                                     sw128_desc(vb + kk * T::UMMA_K * 128, T::BLK_BYTES, 1024), T::IDESC_PV,
+                                     (!first || kk > 0) ? 1u : 0u);
                 }
             };
-            // Ring index of K_j / V_j (j absolute), in the producer's load order.
-            auto kidx = [&](int j) { return 2 * (j - kv_lo); };
-            auto active = [&](int g, int j) { return n_t[g] > 0 && j >= lo_t[g] && j < lo_t[g] + n_t[g]; };
+            // P_g of the item's key tile j (relative to the tile's first) is ready
+            auto wait_p = [&](int g, int jrel) {
+                return wait_warp(b_p_full + 8u * g, ((g ? pdone1 : pdone0) + jrel) & 1, abort_flag, prm.st,
+                                 SITE_P_FULL);
+            };
+            auto active = [&](int g, int j) {
+                return it.n(g) > 0 && j >= it.lo(g) && j < it.lo(g) + it.n(g);
+            };
             // Both query tiles start at kv_lo (no mask, causal, split): the tiles
             // differ only in where they stop, and the loop runs on relative indices.
             auto run_aligned = [&]() -> bool {
-                if (!wait_kv(0)) return false;
+                const int kv_lo = it.kv_lo;
+                if (!wait_kv(kidx(kv_lo))) return false;
                 tc_fence_after();
-                if (n_t[0] > 0) issue_s(0, kv_lo);
-                if (n_t[1] > 0) issue_s(1, kv_lo);
-                mma_commit_warp(b_kv_empty(0));
-                for (int j = 0; j < n_kv; ++j) {
+                if (it.n(0) > 0) issue_s(0, kv_lo);
+                if (it.n(1) > 0) issue_s(1, kv_lo);
+                mma_commit_warp(b_kv_empty(kidx(kv_lo) % T::KV_SLOTS));
+                for (int j = 0; j < it.n_kv; ++j) {
                     bool v_ready = false, k_next_ready = false;
-                    if (j < n_t[0]) {
-                        if (!wait_warp(b_p_full, j & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
-                        if (!wait_kv(2 * j + 1)) return false;
+                    if (j < it.n(0)) {
+                        if (!wait_p(0, j)) return false;
+                        if (!wait_kv(kidx(kv_lo + j) + 1)) return false;
                         v_ready = true;
                         tc_fence_after();
                         issue_pv(0, kv_lo + j, j == 0);
-                        if (j + 1 < n_t[0]) {
-                            if (!wait_kv(2 * j + 2)) return false;
+                        if (j + 1 < it.n(0)) {
+                            if (!wait_kv(kidx(kv_lo + j + 1))) return false;
                             k_next_ready = true;
                             tc_fence_after();
                             issue_s(0, kv_lo + j + 1);
@@ -277,32 +317,29 @@ __global__ void __launch_bounds__(320, 1)
                             mma_commit_warp(b_o_full);
                         }
                     }
-                    if (j < n_t[1]) {
-                        if (!wait_warp(b_p_full + 8u, j & 1, abort_flag, prm.st, SITE_P_FULL))
-                            return false;
-                        if (!v_ready && !wait_kv(2 * j + 1)) return false;
+                    if (j < it.n(1)) {
+                        if (!wait_p(1, j)) return false;
+                        if (!v_ready && !wait_kv(kidx(kv_lo + j) + 1)) return false;
                         tc_fence_after();
                         issue_pv(1, kv_lo + j, j == 0);
                     }
-                    mma_commit_warp(b_kv_empty((2 * j + 1) % T::KV_SLOTS));  // V_j consumed
-                    if (j < n_t[1]) {
-                        if (j + 1 < n_t[1]) {
-                            if (!k_next_ready && !wait_kv(2 * j + 2)) return false;
+                    mma_commit_warp(b_kv_empty((kidx(kv_lo + j) + 1) % T::KV_SLOTS));  // V_j consumed
+                    if (j < it.n(1)) {
+                        if (j + 1 < it.n(1)) {
+                            if (!k_next_ready && !wait_kv(kidx(kv_lo + j + 1))) return false;
                             tc_fence_after();
                             issue_s(1, kv_lo + j + 1);
                         } else {
                             mma_commit_warp(b_o_full + 8u);
                         }
                     }
-                    if (j + 1 < n_kv) mma_commit_warp(b_kv_empty((2 * j + 2) % T::KV_SLOTS));  // K_{j+1}
+                    if (j + 1 < it.n_kv)
+                        mma_commit_warp(b_kv_empty(kidx(kv_lo + j + 1) % T::KV_SLOTS));  // K_{j+1}
                 }
                 return true;
             };
-            auto run = [&]() -> bool {
-                if (!wait_warp(b_q, 0, abort_flag, prm.st, SITE_Q)) return false;
-                if (n_kv == 0) return true;
-                if ((n_t[0] == 0 || lo_t[0] == kv_lo) && (n_t[1] == 0 || lo_t[1] == kv_lo))
-                    return run_aligned();
+            auto run_general = [&]() -> bool {
+                const int kv_lo = it.kv_lo, n_kv = it.n_kv;
                 if (!wait_kv(kidx(kv_lo))) return false;
                 tc_fence_after();
                 if (active(0, kv_lo)) issue_s(0, kv_lo);
@@ -319,12 +356,11 @@ __global__ void __launch_bounds__(320, 1)
                     };
                     // query tile 0: PV_0(j), then S_0(j+1)
                     if (active(0, j)) {
-                        if (!wait_warp(b_p_full, (j - lo_t[0]) & 1, abort_flag, prm.st, SITE_P_FULL))
-                            return false;
+                        if (!wait_p(0, j - it.lo(0))) return false;
                         if (!wait_kv(kidx(j) + 1)) return false;
                         v_ready = true;
                         tc_fence_after();
-                        issue_pv(0, j, j == lo_t[0]);
+                        issue_pv(0, j, j == it.lo(0));
                         if (active(0, j + 1)) {
                             if (!need_k_next()) return false;
                             tc_fence_after();
@@ -339,12 +375,11 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     // query tile 1: PV_1(j), release V_j, then S_1(j+1)
                     if (active(1, j)) {
-                        if (!wait_warp(b_p_full + 8u, (j - lo_t[1]) & 1, abort_flag, prm.st, SITE_P_FULL))
-                            return false;
+                        if (!wait_p(1, j - it.lo(1))) return false;
                         if (!v_ready && !wait_kv(kidx(j) + 1)) return false;
                         v_ready = true;
                         tc_fence_after();
-                        issue_pv(1, j, j == lo_t[1]);
+                        issue_pv(1, j, j == it.lo(1));
                     }
                     if (!v_ready && !wait_kv(kidx(j) + 1)) return false;  // loaded, never used
                     mma_commit_warp(b_kv_empty((kidx(j) + 1) % T::KV_SLOTS));  // V_j consumed
@@ -368,7 +403,22 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 return true;
             };
-            run();
+            int k = 0;
+            for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+                it = item_info(item);
+                if (!wait_warp(b_q, k & 1, abort_flag, prm.st, SITE_Q)) break;
+                if (it.n_kv > 0) {
+                    const bool aligned = (it.n(0) == 0 || it.lo(0) == it.kv_lo) &&
+                                         (it.n(1) == 0 || it.lo(1) == it.kv_lo);
+                    if (!(aligned ? run_aligned() : run_general())) break;
+                }
+                // Every product of this item that reads Q has been issued; once they are
+                // done the producer may load the next item's Q tiles.
+                mma_commit_warp(b_q_empty);
+                ring += 2 * it.n_kv;
+                pdone0 += it.n0;
+                pdone1 += it.n1;
+            }
             // Every MMA issued above must finish before tensor memory is freed.
             mma_commit_warp(b_done);
             wait_drain(b_done, 0, prm.st, SITE_DRAIN);
@@ -378,14 +428,20 @@ __global__ void __launch_bounds__(320, 1)
         const int g = warp >> 2;         // query tile of this warpgroup
         const int wq = warp & 3;         // lane quarter of tensor memory
         const int row = wq * 32 + lane;  // row within the tile
-        const int q_row = (2 * pair + g) * kTile + row;
-        const int n = g ? n_t[1] : n_t[0];
-        const int jt0 = g ? lo_t[1] : lo_t[0];  // first key tile of this query tile
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tS = tmem + (g ? T::COL_S1 : T::COL_S0) + lane_off;
         const uint32_t tO = tmem + (g ? T::COL_O1 : T::COL_O0) + lane_off;
         const uint32_t b_sf = b_s_full + 8u * g, b_pf = b_p_full + 8u * g, b_of = b_o_full + 8u * g;
         const float cs = prm.cs;
+        int s_seen = 0;  // S tiles of this query tile consumed in earlier items
+        int o_seen = 0;  // outputs of this query tile written in earlier items
+        bool ok = true;
+        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const Item it = item_info(item);
+        const int bh = it.bh, split = it.split, b_idx = it.b_idx, h_idx = it.h_idx;
+        const int q_row = (2 * it.pair + g) * kTile + row;
+        const int n = it.n(g);
+        const int jt0 = it.lo(g);  // first key tile of this query tile
         // keys [key_min, key_max] are visible to this row
         const int key_min = prm.win_left < 0 ? 0 : q_row - prm.win_left;
         const int key_max = prm.win_right < 0 ? N - 1 : min(N - 1, q_row + prm.win_right);
@@ -393,9 +449,8 @@ __global__ void __launch_bounds__(320, 1)
         float m_used = -INFINITY;  // running max in log2 units of the scaled scores
         float l_sum = 0.f;         // running sum of 2^(s*cs - m_used), unrounded (for LSE)
         float l_pv = 0.f;          // the same sum over the rounded P that multiplies V
-        bool ok = true;
         for (int j = 0; j < n; ++j) {
-            if (!wait_warp(b_sf, j & 1, abort_flag, prm.st, SITE_S_FULL)) {
+            if (!wait_warp(b_sf, (s_seen + j) & 1, abort_flag, prm.st, SITE_S_FULL)) {
                 ok = false;
                 break;
             }
@@ -520,7 +575,12 @@ __global__ void __launch_bounds__(320, 1)
             for (int c = 0; c < D / 4; ++c) op[c] = make_float4(0.f, 0.f, 0.f, 0.f);
             prm.lse_part[(static_cast<size_t>(split) * prm.BH + bh) * N + q_row] = -INFINITY;
         }
-        const bool o_ready = ok && n > 0 && wait_warp(b_of, 0, abort_flag, prm.st, SITE_O_FULL);
+        s_seen += n;
+        const bool o_ready = ok && n > 0 && wait_warp(b_of, o_seen & 1, abort_flag, prm.st, SITE_O_FULL);
+        if (n > 0) {
+            ++o_seen;
+            if (!o_ready) ok = false;
+        }
         if (o_ready && split_mode) {
             // fp32 partial for the combine kernel: O over this split's keys, and its LSE
             tc_fence_after();
@@ -572,6 +632,7 @@ __global__ void __launch_bounds__(320, 1)
                 prm.lse[static_cast<size_t>(bh) * N + q_row] =
                     l_sum > 0.f ? (m_used + log2f(l_sum)) * kLn2 : INFINITY;
         }
+        }  // items
     }
 
     // ---- teardown: all tensor-memory traffic of this CTA is complete ----
@@ -629,7 +690,20 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     static const cudaError_t attr = cudaFuncSetAttribute(
         fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
-    const long long grid = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
+    // Items of equal size (no causal mask): persistent CTAs, one per SM (shared memory
+    // admits one), each looping over items.  Causal items differ in size, and the
+    // hardware's block scheduler handing the longest-first items to whichever SM frees
+    // up balances them better than a fixed assignment: one item per CTA there.
+    const long long items = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
+    long long grid = items;
+    if (p.causal == 0) {
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (sms < grid) grid = sms;
+    }
+    if (grid < 1) return cudaSuccess;
     fwd_kernel<D, FP8><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
