@@ -202,29 +202,14 @@ __global__ void __launch_bounds__(320, 1)
             bool ok = true;
             for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++k) {
                 const Item it = item_info(item);
-                // The previous item's products that read Q have completed.
-                if (k > 0 && !wait_one(b_q_empty, (k - 1) & 1, abort_flag, prm.st, SITE_Q_EMPTY)) {
-                    ok = false;
-                    break;
-                }
-                const int q_tiles = (it.n(0) > 0) + (it.n(1) > 0);
-                mbar_arrive_expect_tx(b_q, q_tiles * T::TILE_BYTES);
-                for (int g = 0; g < 2; ++g) {
-                    if (it.n(g) == 0) continue;
-                    for (int blk = 0; blk < T::NBLK; ++blk)
-                        tma_load_4d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
-                                    blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile, it.h_idx, it.b_idx);
-                }
-                for (int j = 0; j < it.n_kv && ok; ++j) {
+                // K_j, V_j of the item's key tile j into the ring
+                auto load_kv = [&](int j) -> bool {
                     for (int t = 0; t < 2; ++t, ++idx) {  // t = 0: K_j, t = 1: V_j
                         const int slot = idx % T::KV_SLOTS;
                         const int round = idx / T::KV_SLOTS;
                         if (round > 0 &&
-                            !wait_one(b_kv_empty(slot), (round - 1) & 1, abort_flag, prm.st,
-                                      SITE_KV_EMPTY)) {
-                            ok = false;
-                            break;
-                        }
+                            !wait_one(b_kv_empty(slot), (round - 1) & 1, abort_flag, prm.st, SITE_KV_EMPTY))
+                            return false;
                         mbar_arrive_expect_tx(b_kv_full(slot), T::TILE_BYTES);
                         const CUtensorMap* map = t ? &tm_v : &tm_k;
                         for (int blk = 0; blk < T::NBLK; ++blk)
@@ -232,7 +217,27 @@ __global__ void __launch_bounds__(320, 1)
                                         b_kv_full(slot), blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile,
                                         it.hk_idx, it.b_idx);
                     }
+                    return true;
+                };
+                // The item's first key tile goes out while the previous item finishes;
+                // its Q tiles once the previous item's products that read Q are done.
+                if (it.n_kv > 0 && !load_kv(0)) {
+                    ok = false;
+                    break;
                 }
+                if (k > 0 && !wait_one(b_q_empty, (k - 1) & 1, abort_flag, prm.st, SITE_Q_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                const int q_tiles = (it.n0 > 0) + (it.n1 > 0);
+                mbar_arrive_expect_tx(b_q, q_tiles * T::TILE_BYTES);
+                for (int g = 0; g < 2; ++g) {
+                    if (it.n(g) == 0) continue;
+                    for (int blk = 0; blk < T::NBLK; ++blk)
+                        tma_load_4d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
+                                    blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile, it.h_idx, it.b_idx);
+                }
+                for (int j = 1; j < it.n_kv && ok; ++j) ok = load_kv(j);
             }
             // Let every copy this thread started land before the CTA can exit.
             if (k > 0) wait_drain(b_q, (k - 1) & 1, prm.st, SITE_DRAIN);
@@ -293,12 +298,18 @@ __global__ void __launch_bounds__(320, 1)
             };
             // Both query tiles start at kv_lo (no mask, causal, split): the tiles
             // differ only in where they stop, and the loop runs on relative indices.
+            bool q_released = false;  // the item's q_empty commit has been made
             auto run_aligned = [&]() -> bool {
                 const int kv_lo = it.kv_lo;
+                const int n_max = max(it.n0, it.n1);
                 if (!wait_kv(kidx(kv_lo))) return false;
                 tc_fence_after();
                 if (it.n(0) > 0) issue_s(0, kv_lo);
                 if (it.n(1) > 0) issue_s(1, kv_lo);
+                if (n_max == 1) {  // no further product reads Q
+                    mma_commit_warp(b_q_empty);
+                    q_released = true;
+                }
                 mma_commit_warp(b_kv_empty(kidx(kv_lo) % T::KV_SLOTS));
                 for (int j = 0; j < it.n_kv; ++j) {
                     bool v_ready = false, k_next_ready = false;
@@ -332,6 +343,10 @@ __global__ void __launch_bounds__(320, 1)
                         } else {
                             mma_commit_warp(b_o_full + 8u);
                         }
+                    }
+                    if (j + 2 == n_max) {  // the item's last S products have just been issued
+                        mma_commit_warp(b_q_empty);
+                        q_released = true;
                     }
                     if (j + 1 < it.n_kv)
                         mma_commit_warp(b_kv_empty(kidx(kv_lo + j + 1) % T::KV_SLOTS));  // K_{j+1}
@@ -406,6 +421,7 @@ __global__ void __launch_bounds__(320, 1)
             int k = 0;
             for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
                 it = item_info(item);
+                q_released = false;
                 if (!wait_warp(b_q, k & 1, abort_flag, prm.st, SITE_Q)) break;
                 if (it.n_kv > 0) {
                     const bool aligned = (it.n(0) == 0 || it.lo(0) == it.kv_lo) &&
@@ -414,7 +430,7 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 // Every product of this item that reads Q has been issued; once they are
                 // done the producer may load the next item's Q tiles.
-                mma_commit_warp(b_q_empty);
+                if (!q_released) mma_commit_warp(b_q_empty);
                 ring += 2 * it.n_kv;
                 pdone0 += it.n0;
                 pdone1 += it.n1;
