@@ -256,8 +256,12 @@ __global__ void __launch_bounds__(320, 1)
             Item it{};        // the item being issued
             int ring = 0;     // ring position of the item's first K tile (K/V loads before it)
             int pdone0 = 0, pdone1 = 0;  // P tiles of query tile 0 / 1 consumed in earlier items
-            auto slot_addr = [&](int idx) {
-                return skv_base + static_cast<uint32_t>((idx % T::KV_SLOTS) * T::TILE_BYTES);
+            // Descriptors as words: per instruction only a constant is added to the low word.
+            const SmemDesc dq0 = sw128_desc_words(sq_base, 16, 1024);              // Q, K-major
+            const SmemDesc dk0 = sw128_desc_words(skv_base, 16, 1024);             // K tiles, K-major
+            const SmemDesc dv0 = sw128_desc_words(skv_base, T::BLK_BYTES, 1024);   // V tiles, MN-major
+            auto slot_desc = [&](SmemDesc base, int idx) {
+                return desc_add(base, static_cast<uint32_t>((idx % T::KV_SLOTS) * T::TILE_BYTES));
             };
             auto wait_kv = [&](int idx) {
                 return wait_warp(b_kv_full(idx % T::KV_SLOTS), (idx / T::KV_SLOTS) & 1, abort_flag,
@@ -267,24 +271,24 @@ __global__ void __launch_bounds__(320, 1)
             auto kidx = [&](int j) { return ring + 2 * (j - it.kv_lo); };
             // S_g = Q_g K_j^T : both operands K-major, 32 bytes of K per instruction.
             auto issue_s = [&](int g, int j) {
-                const uint32_t qa = sq_base + g * T::TILE_BYTES;
-                const uint32_t kb = slot_addr(kidx(j));
+                const SmemDesc qa = desc_add(dq0, static_cast<uint32_t>(g * T::TILE_BYTES));
+                const SmemDesc kb = slot_desc(dk0, kidx(j));
 #pragma unroll
                 for (int kk = 0; kk < D / T::UMMA_K; ++kk) {
                     const uint32_t off = (kk * 32) / 128 * T::BLK_BYTES + (kk * 32) % 128;
-                    mma_ss_warp<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), sw128_desc(qa + off, 16, 1024),
-                                     sw128_desc(kb + off, 16, 1024), T::IDESC_S, kk > 0 ? 1u : 0u);
+                    mma_ss_warp<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), desc_add(qa, off), desc_add(kb, off),
+                                     T::IDESC_S, kk > 0 ? 1u : 0u);
                 }
                 mma_commit_warp(b_s_full + 8u * g);
             };
             // O_g += P_g V_j : P from tensor memory, V MN-major (rows = keys).
             auto issue_pv = [&](int g, int j, bool first) {
-                const uint32_t vb = slot_addr(kidx(j) + 1);
+                const SmemDesc vb = slot_desc(dv0, kidx(j) + 1);
 #pragma unroll
                 for (int kk = 0; kk < kTile / T::UMMA_K; ++kk) {
                     mma_ts_warp<FP8>(tmem + (g ? T::COL_O1 : T::COL_O0),
                                      tmem + (g ? T::COL_S1 : T::COL_S0) + kk * 8,
-                                     sw128_desc(vb + kk * T::UMMA_K * 128, T::BLK_BYTES, 1024), T::IDESC_PV,
+                                     desc_add(vb, static_cast<uint32_t>(kk * T::UMMA_K * 128)), T::IDESC_PV,
                                      (!first || kk > 0) ? 1u : 0u);
                 }
             };
