@@ -392,7 +392,9 @@ def run_ours(args):
             api.fwd_fp8(din["q8"], din["k8"], din["v8"], sq, sk, sv, scale=scale,
                         causal=FP8["causal"], o=eo8, lse=else8)
 
-        n_e2e = max(2, min(args.steps, 30))  # the first copy-in and last copy-out are not overlapped
+        # The first copy-in and the last copy-out overlap no compute (about 3.5 ms
+        # together); 100 steps spread them to about 1 % of a step.
+        n_e2e = max(2, min(args.steps, 100))
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
         ev_comp = [torch.cuda.Event() for _ in range(n_e2e)]

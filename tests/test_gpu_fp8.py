@@ -33,3 +33,20 @@ def test_fp8_fwd_matches_oracle(N, causal):
     assert rel_fro(o, o_ref) <= TOL_FP8_RELFRO, rel_fro(o, o_ref)
     # scores are exact fp32 sums of E4M3 products: the log-sum-exp stays tight
     assert max_abs(lse, lse_ref) <= TOL_LSE_ABS, max_abs(lse, lse_ref)
+
+
+def test_fp8_fwd_persistent_many_items():
+    """Without a mask the FP8 forward runs persistent CTAs: 2 x 24 heads x 8
+    query-tile pairs = 384 items, two or three per CTA, each with a ragged last
+    tile, so barrier phases, the key/value ring position and the output
+    accumulators carry over between items.  Sampled heads against the oracle."""
+    B, H, N, d = 2, 24, 2000, 128
+    inp = make_inputs_fp8(B, H, N, d, seed=11)
+    o, lse = run_fp8(inp, False)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    q, k, v = decoded_fp8(inp)
+    scale = 1.0 / np.sqrt(d)
+    for (b, h) in [(0, 0), (B - 1, H - 1), (B // 2, H // 2)]:
+        o_ref, lse_ref, _ = oracle.head_forward(q[b, h], k[b, h], v[b, h], scale, False)
+        assert rel_fro(o[b, h], o_ref) <= TOL_FP8_RELFRO, (b, h, rel_fro(o[b, h], o_ref))
+        assert max_abs(lse[b, h], lse_ref) <= TOL_LSE_ABS, (b, h)
