@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from exact_attention_52_gb300 import api
-from exact_attention_52_gb300.inputs import make_inputs_fp8
+from exact_attention_52_gb300.inputs import AttnInputsFP8, f32_to_e4m3, make_inputs_fp8
 
 from .helpers import (TOL_FP8_RELFRO, TOL_LSE_ABS, decoded_fp8, device_bf16_to_f64,
                       device_f32_to_f64, max_abs, rel_fro, u8_to_device)
@@ -50,3 +50,27 @@ def test_fp8_fwd_persistent_many_items():
         o_ref, lse_ref, _ = oracle.head_forward(q[b, h], k[b, h], v[b, h], scale, False)
         assert rel_fro(o[b, h], o_ref) <= TOL_FP8_RELFRO, (b, h, rel_fro(o[b, h], o_ref))
         assert max_abs(lse[b, h], lse_ref) <= TOL_LSE_ABS, (b, h)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fp8_fwd_growing_scores_exercise_rescale(causal):
+    """Keys that grow along a direction shared with the queries make every row's
+    maximum rise by more than the lazy threshold (2^8 in log2 units) from one key
+    tile to the next: without a mask every row rescales its output accumulator at
+    each of the 7 key tiles after the first (counted on the CPU with the same
+    rule), so the FP8 rescale path runs throughout."""
+    B, H, N, d = 1, 2, 1024, 128
+    rng = np.random.Generator(np.random.PCG64(21))
+    base = rng.standard_normal(d).astype(np.float32)
+    q = (base + 0.5 * rng.standard_normal((B, H, N, d))).astype(np.float32)
+    ramp = (6.0 * np.arange(N) / N).astype(np.float32)[None, None, :, None]
+    k = (ramp * base + 0.5 * rng.standard_normal((B, H, N, d))).astype(np.float32)
+    v = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    (q8, sq), (k8, sk), (v8, sv) = f32_to_e4m3(q), f32_to_e4m3(k), f32_to_e4m3(v)
+    inp = AttnInputsFP8(B, H, N, d, q8, k8, v8, sq, sk, sv, 21)
+    o, lse = run_fp8(inp, causal)
+    qd, kd, vd = decoded_fp8(inp)
+    o_ref, lse_ref = oracle.forward(qd, kd, vd, 1.0 / np.sqrt(d), causal)
+    assert np.all(np.isfinite(o))
+    assert rel_fro(o, o_ref) <= TOL_FP8_RELFRO, rel_fro(o, o_ref)
+    assert max_abs(lse, lse_ref) <= TOL_LSE_ABS, max_abs(lse, lse_ref)
