@@ -270,27 +270,32 @@ __global__ void __launch_bounds__(320, 1)
             // Ring index of K_j / V_j (j absolute), in the producer's load order.
             auto kidx = [&](int j) { return ring + 2 * (j - it.kv_lo); };
             // S_g = Q_g K_j^T : both operands K-major, 32 bytes of K per instruction.
+            // Issued four instructions at a time: instruction kk of quad q reads the
+            // 32 bytes at (4q + kk) * 32 of each row, i.e. block q, byte 32 kk.
             auto issue_s = [&](int g, int j) {
                 const SmemDesc qa = desc_add(dq0, static_cast<uint32_t>(g * T::TILE_BYTES));
                 const SmemDesc kb = slot_desc(dk0, kidx(j));
+                constexpr int QUADS = D / T::UMMA_K / 4;
 #pragma unroll
-                for (int kk = 0; kk < D / T::UMMA_K; ++kk) {
-                    const uint32_t off = (kk * 32) / 128 * T::BLK_BYTES + (kk * 32) % 128;
-                    mma_ss_warp<FP8>(tmem + (g ? T::COL_S1 : T::COL_S0), desc_add(qa, off), desc_add(kb, off),
-                                     T::IDESC_S, kk > 0 ? 1u : 0u);
-                }
+                for (int q = 0; q < QUADS; ++q)
+                    mma_ss_warp4<FP8, 0, 2, 4, 6, 0, 2, 4, 6>(
+                        tmem + (g ? T::COL_S1 : T::COL_S0), desc_add(qa, q * T::BLK_BYTES),
+                        desc_add(kb, q * T::BLK_BYTES), T::IDESC_S, q > 0 ? 1u : 0u);
                 mma_commit_warp(b_s_full + 8u * g);
             };
             // O_g += P_g V_j : P from tensor memory, V MN-major (rows = keys).
+            // Instruction kk reads P columns 8 kk.. and V rows UMMA_K kk.. (UMMA_K
+            // 128-byte rows each); four per quad.
             auto issue_pv = [&](int g, int j, bool first) {
                 const SmemDesc vb = slot_desc(dv0, kidx(j) + 1);
+                constexpr int QUADS = kTile / T::UMMA_K / 4;
+                constexpr uint32_t VS = T::UMMA_K * 8;  // V rows of one instruction, 16-byte units
 #pragma unroll
-                for (int kk = 0; kk < kTile / T::UMMA_K; ++kk) {
-                    mma_ts_warp<FP8>(tmem + (g ? T::COL_O1 : T::COL_O0),
-                                     tmem + (g ? T::COL_S1 : T::COL_S0) + kk * 8,
-                                     desc_add(vb, static_cast<uint32_t>(kk * T::UMMA_K * 128)), T::IDESC_PV,
-                                     (!first || kk > 0) ? 1u : 0u);
-                }
+                for (int q = 0; q < QUADS; ++q)
+                    mma_ts_warp4<FP8, 0, 8, 16, 24, 0, VS, 2 * VS, 3 * VS>(
+                        tmem + (g ? T::COL_O1 : T::COL_O0), tmem + (g ? T::COL_S1 : T::COL_S0) + 32 * q,
+                        desc_add(vb, static_cast<uint32_t>(4 * q * T::UMMA_K * 128)), T::IDESC_PV,
+                        (!first || q > 0) ? 1u : 0u);
             };
             // P_g of the item's key tile j (relative to the tile's first) is ready
             auto wait_p = [&](int g, int jrel) {

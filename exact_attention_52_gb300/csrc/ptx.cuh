@@ -495,6 +495,89 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, Sm
     }
 }
 
+// Four products from one asm block: one elect.sync for the four, the first
+// accumulating as `accumulate` says and the other three always accumulating.
+// The offsets are compile-time constants: OA/OB are added to the low words of
+// the shared-memory descriptors (16-byte units); for the TS form OA is added to
+// the tensor-memory address of A (columns).
+template <bool FP8, uint32_t OA0, uint32_t OA1, uint32_t OA2, uint32_t OA3, uint32_t OB0, uint32_t OB1,
+          uint32_t OB2, uint32_t OB3>
+__device__ __forceinline__ void mma_ss_warp4(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc,
+                                             uint32_t accumulate) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n\t.reg .pred p, t, e;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %5, %5;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "add.u32 al, %1, %7;\n\tadd.u32 bl, %3, %11;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, p;\n\t"
+            "add.u32 al, %1, %8;\n\tadd.u32 bl, %3, %12;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+            "add.u32 al, %1, %9;\n\tadd.u32 bl, %3, %13;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+            "add.u32 al, %1, %10;\n\tadd.u32 bl, %3, %14;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], da, db, %5, t;\n\t"
+            "}"
+            ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate),
+            "n"(OA0), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB0), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p, t, e;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+            "setp.ne.b32 p, %6, 0;\n\tsetp.eq.b32 t, %5, %5;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "add.u32 al, %1, %7;\n\tadd.u32 bl, %3, %11;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t"
+            "add.u32 al, %1, %8;\n\tadd.u32 bl, %3, %12;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+            "add.u32 al, %1, %9;\n\tadd.u32 bl, %3, %13;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+            "add.u32 al, %1, %10;\n\tadd.u32 bl, %3, %14;\n\tmov.b64 da, {al, %2};\n\tmov.b64 db, {bl, %4};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t"
+            "}"
+            ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate),
+            "n"(OA0), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB0), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+    }
+}
+
+template <bool FP8, uint32_t OA0, uint32_t OA1, uint32_t OA2, uint32_t OA3, uint32_t OB0, uint32_t OB1,
+          uint32_t OB2, uint32_t OB3>
+__device__ __forceinline__ void mma_ts_warp4(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
+                                             uint32_t accumulate) {
+    if constexpr (FP8) {
+        asm volatile(
+            "{\n\t.reg .pred p, t, e;\n\t.reg .b32 ta, bl;\n\t.reg .b64 db;\n\t"
+            "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "add.u32 ta, %1, %6;\n\tadd.u32 bl, %2, %10;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %4, p;\n\t"
+            "add.u32 ta, %1, %7;\n\tadd.u32 bl, %2, %11;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %4, t;\n\t"
+            "add.u32 ta, %1, %8;\n\tadd.u32 bl, %2, %12;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %4, t;\n\t"
+            "add.u32 ta, %1, %9;\n\tadd.u32 bl, %2, %13;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [ta], db, %4, t;\n\t"
+            "}"
+            ::"r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate),
+            "n"(OA0), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB0), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p, t, e;\n\t.reg .b32 ta, bl;\n\t.reg .b64 db;\n\t"
+            "setp.ne.b32 p, %5, 0;\n\tsetp.eq.b32 t, %4, %4;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "add.u32 ta, %1, %6;\n\tadd.u32 bl, %2, %10;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, p;\n\t"
+            "add.u32 ta, %1, %7;\n\tadd.u32 bl, %2, %11;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, t;\n\t"
+            "add.u32 ta, %1, %8;\n\tadd.u32 bl, %2, %12;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, t;\n\t"
+            "add.u32 ta, %1, %9;\n\tadd.u32 bl, %2, %13;\n\tmov.b64 db, {bl, %3};\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [ta], db, %4, t;\n\t"
+            "}"
+            ::"r"(d_tmem), "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate),
+            "n"(OA0), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB0), "n"(OB1), "n"(OB2), "n"(OB3)
+            : "memory");
+    }
+}
+
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
