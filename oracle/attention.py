@@ -192,6 +192,22 @@ def head_backward(q, k, v, do, scale, causal, window=None):
     return dq, dk, dv, dsum
 
 
+def head_backward_rows(q, k, v, do, scale, causal, rows, window=None):
+    """dQ for the query rows ``rows`` only, by the same calculus as
+    ``head_backward``: each row of dQ needs only that row of P, dP and D, so long
+    sequences can be checked row by row (``dQ_i = scale * sum_j dS_ij K_j`` with
+    ``dS_i = P_i * (dP_i - D_i)``, ``dP_i = dO_i V^T``, ``D_i = sum_j P_ij dP_ij``).
+
+    Returns (dQ [rows, d], D [rows]).
+    """
+    rows = np.asarray(rows)
+    _, _, p = head_forward(q, k, v, scale, causal, rows=rows, window=window)
+    dp = do[rows] @ v.T
+    dsum = np.sum(p * dp, axis=1)
+    ds = p * (dp - dsum[:, None])
+    return float(scale) * (ds @ k), dsum
+
+
 def backward(q, k, v, do, scale, causal, heads=None):
     """Backward on fp64 ``[B, H, N, d]`` arrays.
 

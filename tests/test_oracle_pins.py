@@ -247,6 +247,43 @@ def test_backward_matches_finite_differences(causal, nq, nk):
 
 
 @pytest.mark.parametrize("causal", [False, True])
+def test_backward_rows_match_finite_differences(causal):
+    """dQ of selected rows against central differences of L = sum(dO * O) in
+    those rows of Q (one is the first row, which sees a single key when causal)."""
+    nq, nk, d = 9, 9, 4
+    q, k, v = rand((nq, d), 130), rand((nk, d), 131), rand((nk, 3), 132)
+    do = rand((nq, 3), 133)
+    scale = 0.7
+    rows = np.array([0, 4, 8])
+    dq_rows, _ = A.head_backward_rows(q, k, v, do, scale, causal, rows)
+
+    def loss(qq):
+        o, _, _ = A.head_forward(qq, k, v, scale, causal)
+        return float(np.sum(do * o))
+
+    h = 1e-6
+    num = np.zeros((len(rows), d))
+    for a, i in enumerate(rows):
+        for c in range(d):
+            qp, qm = q.copy(), q.copy()
+            qp[i, c] += h
+            qm[i, c] -= h
+            num[a, c] = (loss(qp) - loss(qm)) / (2 * h)
+    err = np.linalg.norm(num - dq_rows) / np.linalg.norm(num)
+    assert err < 1e-6, err
+
+
+def test_backward_rows_agree_with_full_backward():
+    N, d = 40, 8
+    q, k, v, do = (rand((N, d), s) for s in (140, 141, 142, 143))
+    dq, _, _, dsum = A.head_backward(q, k, v, do, 0.4, True, window=(6, 0))
+    rows = np.array([0, 7, 39])
+    dq_rows, d_rows = A.head_backward_rows(q, k, v, do, 0.4, True, rows, window=(6, 0))
+    np.testing.assert_allclose(dq_rows, dq[rows], rtol=0, atol=1e-13)
+    np.testing.assert_allclose(d_rows, dsum[rows], rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
 def test_D_identity(causal):
     N, d = 30, 8
     q, k, v, do = (rand((N, d), s) for s in (110, 111, 112, 113))
