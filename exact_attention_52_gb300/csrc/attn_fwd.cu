@@ -26,10 +26,13 @@
 // sections 1-2), adapted to tcgen05: the overlap comes from two query tiles
 // ping-ponging on one MMA issuer instead of register-resident accumulators.
 //
-// The output rescale is lazy: a row's running max m_used is raised only when
-// the tile max exceeds it by more than 2^8 (log2 units), so P <= 256 and O,
-// l share the same stale max, which keeps the result exact ("conditional
-// rescaling" in the FlashAttention-3 walkthrough tags).
+// The output rescale is lazy ("conditional rescaling" in the FlashAttention-3
+// walkthrough tags): O and the row sums always share the same, possibly stale,
+// maximum m_used, which keeps the result exact.  FP8 raises m_used when a tile's
+// maximum exceeds it by more than 2^8 (log2 units), so P <= 256 stays inside
+// E4M3's range.  bf16 computes a tile maximum only while m_used is unset and
+// otherwise lets P exceed 1 (a bf16 value keeps its relative precision at any
+// magnitude); a tile whose row sum passes 2^60 is redone with its own maximum.
 #include <cuda_runtime.h>
 
 #include "attn_internal.h"
@@ -40,6 +43,7 @@ namespace {
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;
+constexpr float kRedoBound = 1152921504606846976.0f;  // 2^60
 
 template <int D, bool FP8>
 struct FwdTraits {
@@ -488,40 +492,55 @@ __global__ void __launch_bounds__(320, 1)
 
             const int kv0 = (jt0 + j) * kTile;
             const int c_lo = key_min - kv0, c_hi = key_max - kv0;  // visible columns [c_lo, c_hi]
-            if (c_lo > 0 || c_hi < kTile - 1) {
+            auto apply_mask = [&]() {
+                if (c_lo > 0 || c_hi < kTile - 1) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            if (c * 32 + i < c_lo || c * 32 + i > c_hi) s[c][i] = f2u(-INFINITY);
+                }
+            };
+            apply_mask();
+            // Running maximum m_used (log2 units; lazy: raised only when a tile's maximum
+            // exceeds it by more than 2^8).  FP8 rows update it on every tile, because
+            // E4M3 P must stay below 448.  bf16 rows compute a tile maximum only while
+            // m_used is still -inf and otherwise exponentiate against m_used: P may then
+            // exceed 1, which costs a bf16 value no relative precision, and a tile whose
+            // row sum passes 2^60 is redone below with its exact maximum, so P, O and the
+            // sums stay far from the fp32 range.
+            float alpha = 1.f;
+            bool rescale_o = false;
+            auto update_max = [&]() {
+                float mx8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mx8[i] = u2f(s[0][i]);
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (c * 32 + i < c_lo || c * 32 + i > c_hi) s[c][i] = f2u(-INFINITY);
-            }
-            float mx8[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx8[i] = u2f(s[0][i]);
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-                for (int i = (c == 0 ? 8 : 0); i < 32; i += 2)
-                    mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], u2f(s[c][i]), u2f(s[c][i + 1]));
-            const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                                   fmaxf(mx8[6], mx8[7]));
-            const float mx_s = mx * cs;
+                    for (int i = (c == 0 ? 8 : 0); i < 32; i += 2)
+                        mx8[(i >> 1) & 7] = fmax3(mx8[(i >> 1) & 7], u2f(s[c][i]), u2f(s[c][i + 1]));
+                const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                                       fmaxf(mx8[6], mx8[7]));
+                const float mx_s = mx * cs;
+                if (mx_s > m_used + kRescaleThreshold) {
+                    alpha = ex2_approx(m_used - mx_s);  // 0 when m_used is still -inf
+                    l_sum *= alpha;
+                    l_pv *= alpha;
+                    m_used = mx_s;
+                    rescale_o = (j > 0);
+                }
+            };
+            if (FP8 || __any_sync(0xffffffffu, m_used == -INFINITY)) update_max();
 
-            float alpha = 1.f;
-            bool rescale_o = false;
-            if (mx_s > m_used + kRescaleThreshold) {
-                alpha = ex2_approx(m_used - mx_s);  // 0 when m_used is still -inf
-                l_sum *= alpha;
-                l_pv *= alpha;
-                m_used = mx_s;
-                rescale_o = (j > 0);
-            }
-            const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
-
-            float ls[4] = {0.f, 0.f, 0.f, 0.f};
-            float lr[4] = {0.f, 0.f, 0.f, 0.f};
-            if constexpr (FP8) {
-                uint32_t pk[32];
+            // P is kept in registers until the tile is accepted: its bf16 words would
+            // overwrite the S columns, which a redo reads again.
+            float ls[4], lr[4];
+            uint32_t pk0[32], pk1[32];  // packed P: FP8 all 128 keys in pk0; bf16 keys 0-63, 64-127
+            auto exp_pass = [&]() {
+                const float m_sub = (m_used == -INFINITY) ? 0.f : m_used;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) ls[e] = lr[e] = 0.f;
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -531,43 +550,43 @@ __global__ void __launch_bounds__(320, 1)
                         ffma2(x2, x3, u2f(s[c][i + 2]), u2f(s[c][i + 3]), cs, cs, -m_sub, -m_sub);
                         const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
                         const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-                        float a0, a1;
-                        fadd2(a0, a1, p0, p1, p2, p3);
-                        fadd2(ls[(i >> 2) & 1], ls[2 + ((i >> 2) & 1)], ls[(i >> 2) & 1],
-                              ls[2 + ((i >> 2) & 1)], a0, a1);
-                        pk[c * 8 + i / 4] = pack_e4m3x4(p0, p1, p2, p3);
-                    }
-                tmem_st32(tS, pk);
-            } else {
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pk[32];
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        const int c = 2 * h + cc;
-#pragma unroll
-                        for (int i = 0; i < 32; i += 4) {
-                            float x0, x1, x2, x3;
-                            ffma2(x0, x1, u2f(s[c][i]), u2f(s[c][i + 1]), cs, cs, -m_sub, -m_sub);
-                            ffma2(x2, x3, u2f(s[c][i + 2]), u2f(s[c][i + 3]), cs, cs, -m_sub, -m_sub);
-                            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                            const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                        if constexpr (FP8) {
+                            pk0[c * 8 + i / 4] = pack_e4m3x4(p0, p1, p2, p3);
+                        } else {
                             const uint32_t w0 = pack_bf16x2(p0, p1), w1 = pack_bf16x2(p2, p3);
                             // The O normaliser sums the same bf16 values that multiply V, so
                             // O stays an exact convex combination of V rows; LSE uses the
                             // unrounded sum.
                             lr[(i >> 2) & 1] = add_bf16x2(lr[(i >> 2) & 1], w0);
                             lr[2 + ((i >> 2) & 1)] = add_bf16x2(lr[2 + ((i >> 2) & 1)], w1);
-                            float a0, a1;
-                            fadd2(a0, a1, p0, p1, p2, p3);
-                            fadd2(ls[(i >> 2) & 1], ls[2 + ((i >> 2) & 1)], ls[(i >> 2) & 1],
-                                  ls[2 + ((i >> 2) & 1)], a0, a1);
-                            pk[cc * 16 + i / 2] = w0;
-                            pk[cc * 16 + i / 2 + 1] = w1;
+                            uint32_t* dst = c < 2 ? pk0 : pk1;
+                            dst[(c & 1) * 16 + i / 2] = w0;
+                            dst[(c & 1) * 16 + i / 2 + 1] = w1;
                         }
+                        float a0, a1;
+                        fadd2(a0, a1, p0, p1, p2, p3);
+                        fadd2(ls[(i >> 2) & 1], ls[2 + ((i >> 2) & 1)], ls[(i >> 2) & 1],
+                              ls[2 + ((i >> 2) & 1)], a0, a1);
                     }
-                    tmem_st32(tS + 32 * h, pk);
+            };
+            exp_pass();
+            if constexpr (!FP8) {
+                const float tile_sum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
+                if (__any_sync(0xffffffffu, !(tile_sum <= kRedoBound))) {
+                    // the scores of this tile rose far above m_used: redo it with its
+                    // maximum (S is still in tensor memory: no P has been stored)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
+                    apply_mask();
+                    update_max();
+                    exp_pass();
                 }
+                tmem_st32(tS, pk0);
+                tmem_st32(tS + 32, pk1);
+            } else {
+                tmem_st32(tS, pk0);
             }
             l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l_pv += (lr[0] + lr[1]) + (lr[2] + lr[3]);

@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 from exact_attention_52_gb300 import api
-from exact_attention_52_gb300.inputs import make_inputs
+from exact_attention_52_gb300.inputs import AttnInputs, f32_to_bf16_bits, make_inputs
 
 from .helpers import (bf16_out_err, TOL_LSE_ABS, TOL_O_MAXABS, bf16_to_device, decoded, device_bf16_to_f64,
                       device_f32_to_f64, max_abs)
@@ -48,8 +48,9 @@ def test_fwd_many_heads_and_batches(causal):
 
 
 def test_fwd_outlier_keys_exercise_rescale():
-    """A few keys scaled x8 raise the running max by far more than the lazy
-    threshold mid-sequence, so the output rescale path runs."""
+    """A few keys scaled x8 raise a row's scores far above its first tile's
+    maximum mid-sequence: P exceeds 1 by up to about 2^35 on those tiles (bf16
+    rows exponentiate against the stored maximum)."""
     inp = make_inputs(1, 4, 1024, 128, seed=3, outlier_frac=0.01, outlier_factor=8.0)
     o, lse = run_fwd(inp, False)
     q, k, v, _ = decoded(inp)
@@ -82,3 +83,29 @@ def test_fwd_identical_value_rows():
     o, _ = run_fwd(inp, False)
     v = oracle.bf16_bits_to_f64(inp.v_bits)
     assert max_abs(o, v) <= 1e-2
+
+
+@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_score_jumps_redo_tiles(causal, d):
+    """Keys that grow along a direction shared with the queries, so that a row's
+    scores rise by tens of log2 units from one 128-key tile to the next: bf16
+    tiles whose row sum against the stored maximum passes 2^60 are redone with
+    their own maximum and the output is rescaled (d = 128: up to 7 redos per row,
+    counted on the CPU with the same rule), and the tiles in between carry P up
+    to about 2^58."""
+    B, H, N = 1, 2, 1024
+    rng = np.random.Generator(np.random.PCG64(31))
+    base = rng.standard_normal(d).astype(np.float32)
+    q = (base + 0.5 * rng.standard_normal((B, H, N, d))).astype(np.float32)
+    ramp = (32.0 * np.arange(N) / N).astype(np.float32)[None, None, :, None]
+    k = (ramp * base + 0.5 * rng.standard_normal((B, H, N, d))).astype(np.float32)
+    v = rng.standard_normal((B, H, N, d)).astype(np.float32)
+    inp = AttnInputs(B, H, N, d, f32_to_bf16_bits(q), f32_to_bf16_bits(k), f32_to_bf16_bits(v),
+                     None, 31, None)
+    o, lse = run_fwd(inp, causal)
+    qd, kd, vd, _ = decoded(inp)
+    o_ref, lse_ref = oracle.forward(qd, kd, vd, 1.0 / np.sqrt(d), causal)
+    assert np.all(np.isfinite(o)) and np.all(np.isfinite(lse))
+    assert bf16_out_err(o, o_ref) <= TOL_O_MAXABS
+    assert max_abs(lse, lse_ref) <= TOL_LSE_ABS, max_abs(lse, lse_ref)
