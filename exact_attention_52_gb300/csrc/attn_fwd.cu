@@ -28,11 +28,11 @@
 //
 // The output rescale is lazy ("conditional rescaling" in the FlashAttention-3
 // walkthrough tags): O and the row sums always share the same, possibly stale,
-// maximum m_used, which keeps the result exact.  FP8 raises m_used when a tile's
-// maximum exceeds it by more than 2^8 (log2 units), so P <= 256 stays inside
-// E4M3's range.  bf16 computes a tile maximum only while m_used is unset and
-// otherwise lets P exceed 1 (a bf16 value keeps its relative precision at any
-// magnitude); a tile whose row sum passes 2^60 is redone with its own maximum.
+// maximum m_used, which keeps the result exact.  A row computes a tile maximum
+// only on its first tile and otherwise lets P exceed 1; a tile whose row sum
+// passes 448 (FP8: then some P could leave E4M3's range) or 2^60 (bf16, which
+// keeps its relative precision at any magnitude) is redone with its own
+// maximum.
 #include <cuda_runtime.h>
 
 #include "attn_internal.h"
@@ -44,6 +44,7 @@ namespace {
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kRedoBound = 1152921504606846976.0f;  // 2^60
+constexpr float kRedoBoundFP8 = 448.0f;                 // largest finite E4M3 value
 
 template <int D, bool FP8>
 struct FwdTraits {
@@ -502,16 +503,16 @@ __global__ void __launch_bounds__(320, 1)
                 }
             };
             apply_mask();
-            // Running maximum m_used (log2 units; lazy: raised only when a tile's maximum
-            // exceeds it by more than 2^8).  FP8 rows update it on every tile, because
-            // E4M3 P must stay below 448.  bf16 rows compute a tile maximum only while
-            // m_used is still -inf and otherwise exponentiate against m_used: P may then
-            // exceed 1, which costs a bf16 value no relative precision, and a tile whose
-            // row sum passes 2^60 is redone below with its exact maximum, so P, O and the
-            // sums stay far from the fp32 range.
+            // Running maximum m_used (log2 units).  A tile maximum is computed only while
+            // m_used is still -inf; later tiles are exponentiated against m_used, so P
+            // may exceed 1.  A tile is redone with its own maximum when its row sum
+            // passes a bound: 448 for FP8 (every P of the tile is at most the sum, and
+            // E4M3 stops at 448), 2^60 for bf16 (a bf16 value keeps its relative
+            // precision at any magnitude; the bound keeps P, O and the sums far inside
+            // fp32).  m_used is raised when the tile maximum exceeds it by more than tau.
             float alpha = 1.f;
             bool rescale_o = false;
-            auto update_max = [&]() {
+            auto update_max = [&](float tau) {
                 float mx8[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) mx8[i] = u2f(s[0][i]);
@@ -523,7 +524,7 @@ __global__ void __launch_bounds__(320, 1)
                 const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
                                        fmaxf(mx8[6], mx8[7]));
                 const float mx_s = mx * cs;
-                if (mx_s > m_used + kRescaleThreshold) {
+                if (mx_s > m_used + tau) {
                     alpha = ex2_approx(m_used - mx_s);  // 0 when m_used is still -inf
                     l_sum *= alpha;
                     l_pv *= alpha;
@@ -531,7 +532,7 @@ __global__ void __launch_bounds__(320, 1)
                     rescale_o = (j > 0);
                 }
             };
-            if (FP8 || __any_sync(0xffffffffu, m_used == -INFINITY)) update_max();
+            if (__any_sync(0xffffffffu, m_used == -INFINITY)) update_max(kRescaleThreshold);
 
             // P is kept in registers until the tile is accepted: its bf16 words would
             // overwrite the S columns, which a redo reads again.
@@ -570,24 +571,22 @@ __global__ void __launch_bounds__(320, 1)
                     }
             };
             exp_pass();
-            if constexpr (!FP8) {
+            {
                 const float tile_sum = (ls[0] + ls[1]) + (ls[2] + ls[3]);
-                if (__any_sync(0xffffffffu, !(tile_sum <= kRedoBound))) {
-                    // the scores of this tile rose far above m_used: redo it with its
-                    // maximum (S is still in tensor memory: no P has been stored)
+                if (__any_sync(0xffffffffu, !(tile_sum <= (FP8 ? kRedoBoundFP8 : kRedoBound)))) {
+                    // the scores of this tile rose above m_used: redo it with its maximum
+                    // (S is still in tensor memory: no P has been stored)
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld32(tS + 32 * c, s[c]);
 #pragma unroll
                     for (int c = 0; c < 4; ++c) tmem_ld_wait(s[c]);
                     apply_mask();
-                    update_max();
+                    update_max(0.f);
                     exp_pass();
                 }
-                tmem_st32(tS, pk0);
-                tmem_st32(tS + 32, pk1);
-            } else {
-                tmem_st32(tS, pk0);
             }
+            tmem_st32(tS, pk0);
+            if constexpr (!FP8) tmem_st32(tS + 32, pk1);
             l_sum += (ls[0] + ls[1]) + (ls[2] + ls[3]);
             l_pv += (lr[0] + lr[1]) + (lr[2] + lr[3]);
             if (__any_sync(0xffffffffu, rescale_o)) {
