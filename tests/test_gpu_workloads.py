@@ -11,7 +11,7 @@ import oracle
 from exact_attention_52_gb300 import api
 from exact_attention_52_gb300.inputs import workload_inputs, WORKLOADS
 
-from .helpers import (bf16_out_err, TOL_FP8_RELFRO, TOL_GRAD_RELFRO, TOL_LSE_ABS, TOL_O_MAXABS, bf16_to_device,
+from .helpers import (bf16_half_ulp, bf16_out_err, TOL_FP8_RELFRO, TOL_GRAD_RELFRO, TOL_LSE_ABS, TOL_O_MAXABS, bf16_to_device,
                       decoded, decoded_fp8, device_bf16_to_f64, device_f32_to_f64, max_abs,
                       rel_fro, u8_to_device)
 
@@ -67,6 +67,13 @@ def test_large_bf16_workloads_sampled_heads(name, heads):
     ks = k.reshape(-1, w["N"], w["d"])
     diag = scale * np.einsum("hnd,hnd->hn", qs, ks)
     assert np.all(lg.reshape(diag.shape) >= diag - TOL_LSE_ABS)
+    # every head and row: O is a convex combination of the head's V rows, so each
+    # element lies within that head's range of the V column (up to the tolerance
+    # and the output's own rounding)
+    vmin = v.min(axis=2, keepdims=True)
+    vmax = v.max(axis=2, keepdims=True)
+    slack = TOL_O_MAXABS + bf16_half_ulp(np.maximum(np.abs(vmin), np.abs(vmax)))
+    assert np.all(og >= vmin - slack) and np.all(og <= vmax + slack)
 
 
 def test_fp8_workload_sampled_rows():
