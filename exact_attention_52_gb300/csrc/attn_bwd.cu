@@ -326,7 +326,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     } else if (warp == 13) {
         // ================= MMA issuer =================
-        if (lane == 0) {
+        // The whole warp walks the schedule; one elected lane issues each group of
+        // four products (uniform operands, one elect.sync per group).
+        __syncwarp();
+        {
             const uint32_t tDV = tmem + T::COL_DV, tDK = tmem + T::COL_DK;
             const uint32_t sK = sbase + T::OFF_K, sV = sbase + T::OFF_V, sDS = sbase + T::OFF_DS;
             // K-major operand, 16 bf16 (32 bytes) of K per instruction.
@@ -338,77 +341,77 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 return desc_add(sw128_desc_words(base, T::BLK_BYTES, 1024), kk * 16 * 128);
             };
             auto run = [&]() -> bool {
-                if (!wait_one(b_kv, 0, abort_flag, prm.st, SITE_KV)) return false;
+                if (!wait_warp(b_kv, 0, abort_flag, prm.st, SITE_KV)) return false;
                 for (int t = 0; t < n_steps; ++t) {
                     const int s = t % T::STAGES;
                     const uint32_t sQ = sbase + T::OFF_Q + s * T::TILE_BYTES;
                     const uint32_t sDO = sbase + T::OFF_DO + s * T::TILE_BYTES;
-                    if (!wait_one(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL))
+                    if (!wait_warp(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL))
                         return false;
                     tc_fence_after();
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t tR = tmem + h * T::COL_REGION;
                         // S^T_h = K Q_h^T  (M = 128 keys, N = 64 queries, K = d)
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss_bf16(tR, kmaj(sK, kk), kmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_SDP,
-                                          kk > 0);
+                        for (int q = 0; q < D / 64; ++q)
+                            mma_ss_warp4<false, 0, 2, 4, 6, 0, 2, 4, 6>(
+                                tR, kmaj(sK, 4 * q), kmaj(sQ + h * T::HALF_BYTES, 4 * q), T::IDESC_SDP,
+                                q > 0 ? 1u : 0u);
                         if (t > 0 && h < T::NDQ) {  // dQ part h of the previous tile has left
-                            if (!wait_one(b_dq_empty + 8u * h, (t - 1) & 1, abort_flag, prm.st,
-                                          SITE_DQ_EMPTY))
+                            if (!wait_warp(b_dq_empty + 8u * h, (t - 1) & 1, abort_flag, prm.st,
+                                           SITE_DQ_EMPTY))
                                 return false;
                             tc_fence_after();
                         }
                         // dP^T_h = V dO_h^T
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk)
-                            mma_ss_bf16(tR + T::COL_DP, kmaj(sV, kk), kmaj(sDO + h * T::HALF_BYTES, kk),
-                                          T::IDESC_SDP, kk > 0);
-                        mma_commit(b_s_full + 8u * h);
+                        for (int q = 0; q < D / 64; ++q)
+                            mma_ss_warp4<false, 0, 2, 4, 6, 0, 2, 4, 6>(
+                                tR + T::COL_DP, kmaj(sV, 4 * q), kmaj(sDO + h * T::HALF_BYTES, 4 * q),
+                                T::IDESC_SDP, q > 0 ? 1u : 0u);
+                        mma_commit_warp(b_s_full + 8u * h);
                     }
                     for (int h = 0; h < 2; ++h) {
-                        if (!wait_one(b_p_full + 8u * h, t & 1, abort_flag, prm.st, SITE_P_FULL))
+                        if (!wait_warp(b_p_full + 8u * h, t & 1, abort_flag, prm.st, SITE_P_FULL))
                             return false;
                         tc_fence_after();
                         const uint32_t tR = tmem + h * T::COL_REGION;
                         // dV += P^T_h dO_h : A = P^T_h (tensor memory), B = dO_h (MN-major)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ts_bf16(tDV, tR + kk * 8, mnmaj(sDO + h * T::HALF_BYTES, kk),
-                                          T::IDESC_DVK, (t > 0 || h > 0 || kk > 0));
+                        mma_ts_warp4<false, 0, 8, 16, 24, 0, 128, 256, 384>(
+                            tDV, tR, mnmaj(sDO + h * T::HALF_BYTES, 0), T::IDESC_DVK, (t > 0 || h > 0) ? 1u : 0u);
                         // dK += dS^T_h Q_h : A = dS^T block h (K-major), B = Q_h (MN-major)
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_ss_bf16(tDK, kmaj(sDS + h * T::BLK_BYTES, kk),
-                                          mnmaj(sQ + h * T::HALF_BYTES, kk), T::IDESC_DVK,
-                                          (t > 0 || h > 0 || kk > 0));
+                        mma_ss_warp4<false, 0, 2, 4, 6, 0, 128, 256, 384>(
+                            tDK, kmaj(sDS + h * T::BLK_BYTES, 0), mnmaj(sQ + h * T::HALF_BYTES, 0), T::IDESC_DVK,
+                            (t > 0 || h > 0) ? 1u : 0u);
                         if constexpr (D == 128) {
                             // dQ^T for the 64 queries of half h = K^T dS^T_h (M = d, N = 64,
                             // K = keys), into the dP^T columns of region h, issued as soon as
                             // dS^T_h exists rather than after both halves
 #pragma unroll
-                            for (int kk = 0; kk < kTile / 16; ++kk)
-                                mma_ss_bf16(tR + T::COL_DP, mnmaj(sK, kk), mnmaj(sDS + h * T::BLK_BYTES, kk),
-                                              T::IDESC_DQ, kk > 0);
-                            mma_commit(b_dq_full + 8u * h);
+                            for (int q = 0; q < kTile / 64; ++q)
+                                mma_ss_warp4<false, 0, 128, 256, 384, 0, 128, 256, 384>(
+                                    tR + T::COL_DP, mnmaj(sK, 4 * q), mnmaj(sDS + h * T::BLK_BYTES, 4 * q),
+                                    T::IDESC_DQ, q > 0 ? 1u : 0u);
+                            mma_commit_warp(b_dq_full + 8u * h);
                         }
                     }
                     // d = 64: dQ_i = dS K (M = queries, N = d) into the dP^T columns of region 0
 #pragma unroll
                     for (int p = 0; p < (D == 128 ? 0 : T::NDQ); ++p) {
 #pragma unroll
-                        for (int kk = 0; kk < kTile / 16; ++kk)
-                            mma_ss_bf16(tmem + p * T::COL_REGION + T::COL_DP, mnmaj(sDS, kk),
-                                          mnmaj(sK + p * T::BLK_BYTES, kk), T::IDESC_DQ, kk > 0);
-                        mma_commit(b_dq_full + 8u * p);
+                        for (int q = 0; q < kTile / 64; ++q)
+                            mma_ss_warp4<false, 0, 128, 256, 384, 0, 128, 256, 384>(
+                                tmem + p * T::COL_REGION + T::COL_DP, mnmaj(sDS, 4 * q),
+                                mnmaj(sK + p * T::BLK_BYTES, 4 * q), T::IDESC_DQ, q > 0 ? 1u : 0u);
+                        mma_commit_warp(b_dq_full + 8u * p);
                     }
-                    mma_commit(b_qdo_empty(s));
+                    mma_commit_warp(b_qdo_empty(s));
                 }
-                mma_commit(b_dkv_full);
+                mma_commit_warp(b_dkv_full);
                 return true;
             };
             run();
-            mma_commit(b_done);
+            mma_commit_warp(b_done);
             wait_drain(b_done, 0, prm.st, SITE_DRAIN);
         }
     } else if (warp < 8) {

@@ -292,14 +292,6 @@ __host__ __device__ constexpr uint32_t make_idesc(uint32_t ab_format, int M, int
 constexpr uint32_t kFmtBF16 = 1;
 constexpr uint32_t kFmtE4M3 = 0;
 
-// Arrive (once) on `bar` when every tcgen05.mma issued so far by this thread
-// has completed.
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-        : "memory");
-}
-
 // A shared-memory descriptor kept as its two 32-bit words.  The start address
 // sits in the low word (bits 0-13, address >> 4), so a byte offset b is added
 // as lo + (b >> 4): shared memory is below 256 KB, so the field never carries.
@@ -314,26 +306,6 @@ __device__ __forceinline__ SmemDesc sw128_desc_words(uint32_t saddr, uint32_t lb
 
 __device__ __forceinline__ SmemDesc desc_add(SmemDesc d, uint32_t byte_offset) {
     return SmemDesc{d.lo + (byte_offset >> 4), d.hi};
-}
-
-// bf16 products with the descriptors passed as words (fewer instructions per
-// issue than building the 64-bit descriptor each time).
-__device__ __forceinline__ void mma_ss_bf16(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 da, db;\n\tmov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
-        "setp.ne.b32 p, %6, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, p;\n\t}" ::"r"(d_tmem),
-        "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_ts_bf16(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b64 db;\n\tmov.b64 db, {%2, %3};\n\t"
-        "setp.ne.b32 p, %5, 0;\n\ttcgen05.mma.cta_group::1.kind::f16 [%0], [%1], db, %4, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "r"(b.lo), "r"(b.hi), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // Warp-wide forms: every lane of a converged warp executes the call with the
@@ -426,6 +398,9 @@ __device__ __forceinline__ void mma_ts_warp4(uint32_t d_tmem, uint32_t a_tmem, S
     }
 }
 
+// Arrive (once) on `bar` when every tcgen05.mma issued so far by the issuing
+// lane has completed.  elect.sync over a full, converged warp picks the same
+// lane every time, so that lane has issued every product of the warp.
 __device__ __forceinline__ void mma_commit_warp(uint32_t bar) {
     asm volatile(
         "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
