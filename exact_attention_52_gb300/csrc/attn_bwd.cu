@@ -36,8 +36,9 @@
 // one 128-byte line of the accumulator.  d = 64: dQ_i = dS K once per step
 // (lane = query row), staged and TMA-reduced.
 // Shared memory: K, V, two stages of (Q, dO, LSE2, D), and dS^T (bf16,
-// 128-byte swizzle), which serves as the K-major A operand of dK and, read
-// MN-major, as an operand of the dQ product.
+// 128-byte swizzle), read MN-major by the dQ product.  dK takes dS^T from
+// tensor memory instead (packed into the dP^T_h columns the compute warps
+// have just read), so that product reads only Q from shared memory.
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -379,9 +380,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         // dV += P^T_h dO_h : A = P^T_h (tensor memory), B = dO_h (MN-major)
                         mma_ts_warp4<false, 0, 8, 16, 24, 0, 128, 256, 384>(
                             tDV, tR, mnmaj(sDO + h * T::HALF_BYTES, 0), T::IDESC_DVK, (t > 0 || h > 0) ? 1u : 0u);
-                        // dK += dS^T_h Q_h : A = dS^T block h (K-major), B = Q_h (MN-major)
-                        mma_ss_warp4<false, 0, 2, 4, 6, 0, 128, 256, 384>(
-                            tDK, kmaj(sDS + h * T::BLK_BYTES, 0), mnmaj(sQ + h * T::HALF_BYTES, 0), T::IDESC_DVK,
+                        // dK += dS^T_h Q_h : A = dS^T_h (tensor memory), B = Q_h (MN-major)
+                        // (dS^T_h packed in the first columns of dP^T_h, 8 per instruction;
+                        // the dQ product that reuses those columns is issued after it)
+                        mma_ts_warp4<false, 0, 8, 16, 24, 0, 128, 256, 384>(
+                            tDK, tR + T::COL_DP, mnmaj(sQ + h * T::HALF_BYTES, 0), T::IDESC_DVK,
                             (t > 0 || h > 0) ? 1u : 0u);
                         if constexpr (D == 128) {
                             // dQ^T for the 64 queries of half h = K^T dS^T_h (M = d, N = 64,
@@ -483,8 +486,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         dsw[(e + h2) / 2] = pack_bf16x2(d0, d1);
                     }
                 }
-                // P^T chunk -> columns [16 cc, 16 cc + 16) of S^T_h (already read)
+                // P^T chunk -> columns [16 cc, 16 cc + 16) of S^T_h (already read), and
+                // the dS^T chunk likewise into dP^T_h: the A operand of dK from tensor
+                // memory, so that product reads only Q from shared memory
                 tmem_st16(tS + 16 * cc, pk);
+                tmem_st16(tDP + 16 * cc, dsw);
                 // dS^T row r, 64 bytes -> 16-byte chunks x = 4 cc .. 4 cc + 3, swizzled
 #pragma unroll
                 for (int v = 0; v < 4; ++v)
