@@ -90,56 +90,125 @@ def recorded_traffic(kernel_key):
 
 
 class ClockSampler:
-    """nvidia-smi clock / throttle-reason samples during the timed region."""
+    """SM clock, power and throttle-reason samples during the timed region.
 
+    Read-only NVML queries (ctypes on the driver's libnvidia-ml) from a thread
+    every ``period_s`` (5 ms), so that a region of tens of milliseconds still
+    gets a dozen samples or more; the GPU is found by its PCI bus id, which
+    NVML and CUDA share whatever the device numbering.  Falls back to
+    ``nvidia-smi -lms 20`` when NVML cannot be opened.  Nothing is set."""
+
+    # nvmlClocksEventReasons bits
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
               "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
               "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, index):
-        self.index = index
+    def __init__(self, torch_device_index, period_s=0.005):
+        self.index = torch_device_index
+        self.period = period_s
+        self.samples = []  # (sm_mhz, max_mhz, reason bits)
+        self.thread = None
+        self.stop_flag = False
         self.proc = None
         self.path = None
+        self.source = None
+
+    def _bus_id(self):
+        import torch
+        p = torch.cuda.get_device_properties(self.index)
+        try:
+            return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except AttributeError:
+            return None
+
+    def _open_nvml(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        bus = self._bus_id()
+        if bus is None or nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        reasons_fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        return nv, h, reasons_fn
 
     def start(self):
+        import ctypes
+        import threading
+        try:
+            nv, h, reasons_fn = self._open_nvml()
+        except (OSError, AttributeError):
+            return self._start_smi()
+        self.source = "nvml"
+        mx = ctypes.c_uint(0)
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))  # NVML_CLOCK_SM
+
+        def loop():
+            clk = ctypes.c_uint(0)
+            rs = ctypes.c_ulonglong(0)
+            while not self.stop_flag:
+                if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                    r = rs.value if reasons_fn(h, ctypes.byref(rs)) == 0 else 0
+                    self.samples.append((float(clk.value), float(mx.value), r))
+                time.sleep(self.period)
+
+        self.thread = threading.Thread(target=loop, daemon=True)
+        self.thread.start()
+
+    def _start_smi(self):
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
+        bus = self._bus_id()
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                ["nvidia-smi", "-i", bus or str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            self.source = "nvidia-smi"
         except OSError:
             self.proc = None
 
     def stop(self):
-        if self.proc is None:
+        if self.thread is not None:
+            self.stop_flag = True
+            self.thread.join(timeout=5)
+            sm = [x[0] for x in self.samples]
+            mx = [x[1] for x in self.samples]
+            reasons = sorted({n for x in self.samples for bit, n in self.REASONS.items() if x[2] & bit})
+        elif self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            sm, mx, reasons = [], [], set()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 7:
+                        continue
+                    try:
+                        sm.append(float(parts[0]))
+                        mx.append(float(parts[1]))
+                    except ValueError:
+                        continue
+                    for n, v in zip(names, parts[3:7]):
+                        if v.lower() == "active":
+                            reasons.add(n)
+            os.unlink(self.path)
+            reasons = sorted(reasons)
+        else:
             return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        with open(self.path) as f:
-            for line in f:
-                parts = [p.strip() for p in line.split(",")]
-                if len(parts) < 7:
-                    continue
-                try:
-                    sm.append(float(parts[0]))
-                    mx.append(float(parts[1]))
-                except ValueError:
-                    continue
-                for n, v in zip(names, parts[3:7]):
-                    if v.lower() == "active":
-                        reasons.add(n)
-        os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "sm_min_mhz": min(sm),
+                "samples": len(sm), "reasons": reasons, "source": self.source}
 
 
 # ---------------------------------------------------------------------------
@@ -271,6 +340,54 @@ def make_device_data(torch, dev):
     d = {n: t.to(dev) for n, t in h.items()}
     d["scales"] = (f8.sq, f8.sk, f8.sv)
     return h, d
+
+
+def live_gemm_peaks(torch, dev, n=8192, reps=10):
+    """Dense GEMM throughput of this GPU measured now, for the FP8 roofline
+    denominator (no FP8 figure is in the measured-peaks file): cuBLAS through
+    torch, best of ``reps`` n^3 products timed with CUDA events, 2*n^3 flops
+    each.  bf16 is measured the same way, so that the two share one clock and
+    method.  Returns {"fp8_tflops": .., "bf16_tflops": ..} (None where the
+    product is not available)."""
+    out = {"fp8_tflops": None, "bf16_tflops": None, "n": n, "reps": reps,
+           "how": "torch._scaled_mm e4m3 x e4m3 -> bf16 and torch.matmul bf16, "
+                  f"{n}^3, best of {reps}, CUDA events"}
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    a = torch.randn((n, n), device=dev, generator=g, dtype=torch.float32)
+    b = torch.randn((n, n), device=dev, generator=g, dtype=torch.float32)
+
+    def best(fn):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return 2.0 * n ** 3 / (min(ts) * 1e-3) / 1e12
+
+    try:
+        ab, bb = a.to(torch.bfloat16), b.to(torch.bfloat16)
+        out["bf16_tflops"] = round(best(lambda: torch.matmul(ab, bb)), 1)
+        del ab, bb
+    except RuntimeError:
+        pass
+    try:
+        a8 = a.to(torch.float8_e4m3fn)
+        b8 = b.to(torch.float8_e4m3fn).t()  # column-major second operand
+        one = torch.ones((), device=dev, dtype=torch.float32)
+        out["fp8_tflops"] = round(best(lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one,
+                                                                out_dtype=torch.bfloat16)), 1)
+        del a8, b8
+    except (RuntimeError, AttributeError, TypeError):
+        pass
+    del a, b
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -450,18 +567,40 @@ def run_ours(args):
     peaks, peak_kind = load_peaks()
     sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # The timed region lasts tens of milliseconds at the SM clock sampled above:
+    # the burst figure (a GEMM timed alone, best of 10) is the denominator; the
+    # sustained one (seconds under the power cap, at a lower clock) is reported
+    # beside it, labelled.
+    sm_mhz = clk["sm_mhz"] if clk else None
+    live = live_gemm_peaks(torch, dev) if not args.no_live_peaks else {}
+    fp8_peak = live.get("fp8_tflops")
+    fp8_kind = "measured live in this run (cuBLAS e4m3 GEMM)"
+    if not fp8_peak:
+        fp8_peak = 2.0 * burst
+        fp8_kind = f"2 x {peak_kind} bf16 burst (nominal dense FP8/bf16 ratio)"
     bwd_main_flops = flops["bwd"]
     achieved = bwd_main_flops / (k_ms["bwd_main"] * 1e-3) / 1e12
     traffic = recorded_traffic("bwd_main_b1_h32_n8192_d128")
     components = {}
     for name, f, kms in (("fwd", flops["fwd"], k_ms["fwd"]),
                          ("bwd", flops["bwd"], k_ms["bwd_pre"] + k_ms["bwd_main"] + k_ms["bwd_dq_convert"]),
+                         ("bwd_main", flops["bwd"], k_ms["bwd_main"]),
                          ("fwd_fp8", flops["fwd_fp8"], k_ms["fwd_fp8"])):
         tf = f / (kms * 1e-3) / 1e12
-        pk = (2.0 if name == "fwd_fp8" else 1.0)
-        components[name] = {"ms": round(kms, 4), "tflops": round(tf, 1),
-                            "frac_of_sustained": round(tf / (pk * sustained), 4),
-                            "frac_of_burst": round(tf / (pk * burst), 4)}
+        if name == "fwd_fp8":
+            c = {"ms": round(kms, 4), "tflops": round(tf, 1), "frac_of_peak": round(tf / fp8_peak, 4),
+                 "peak_tflops": fp8_peak, "peak_kind": fp8_kind,
+                 "frac_of_2x_bf16_burst": round(tf / (2.0 * burst), 4)}
+        else:
+            c = {"ms": round(kms, 4), "tflops": round(tf, 1), "frac_of_burst": round(tf / burst, 4),
+                 "frac_of_sustained": round(tf / sustained, 4)}
+        if sm_mhz:
+            c["mcycles_at_median_sm_clock"] = round(kms * sm_mhz * 1e-3, 4)
+        components[name] = c
+    secondary = {}
+    if world == 1 and not args.no_secondary:
+        for nm in ("c1_fwd_b1_h1_n128_d64", "c2_fwd_b4_h16_n1024_d64", "c3_causal_b2_h16_n4096_d128"):
+            secondary[nm] = measure_workload(nm, steps=20)[0]
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4),
@@ -470,13 +609,18 @@ def run_ours(args):
         "config": {"workload": WORKLOAD, "l2": "inputs 0.54 GB > 129 MB L2, no flush",
                    "parallelism": f"replicas x{world} (independent heads, no collective)"},
         "components": components,
+        "secondary": secondary or None,
         "kernel_ms": {k: round(v, 4) for k, v in k_ms.items()},
         "roofline": {"kernel": "bwd_main (attn_bwd_main)", "bound": "tensor",
-                     "achieved": round(achieved, 1), "peak": sustained, "unit": "TFLOP/s",
-                     "frac": round(achieved / sustained, 4),
-                     "peak_kind": f"{peak_kind} bf16 sustained (kernel timed inside a long step)",
+                     "achieved": round(achieved, 1), "peak": burst, "unit": "TFLOP/s",
+                     "frac": round(achieved / burst, 4),
+                     "peak_kind": f"{peak_kind} bf16 burst (GEMM timed alone; the timed region "
+                                  f"is {elapsed_ms:.0f} ms at the sampled clock)",
+                     "frac_of_sustained": round(achieved / sustained, 4),
+                     "sustained_peak": sustained,
                      "traffic": traffic,
                      "algorithmic_bytes": attn_bytes(B, H, N, D, "bwd_main")},
+        "live_gemm_peaks": live or None,
         "gpu_launches": len(KERNELS) * args.steps,
         "clocks": clk,
         "cpu_baseline": cpu,
@@ -519,19 +663,24 @@ def window_flops(N, d, left, right):
     return 4.0 * d * float(np.sum(hi - lo + 1))
 
 
-def run_extra(args):
-    """Forward + backward on one of EXTRA_WORKLOADS (a secondary measurement of
-    the grouped-query path; the default run measures the main step)."""
+def measure_workload(name, steps=20, flush_bytes=512 << 20):
+    """Forward (+ backward) of one of EXTRA_WORKLOADS on the current GPU.
+
+    Device time per call between CUDA events on the launching stream, with a
+    write of ``flush_bytes`` (more than the 129 MB L2) before every timed call
+    so that each call reads its inputs from HBM.  Forward-only workloads also
+    report the time per call of back-to-back calls (host-side argument checks
+    and tensor-map encoding included) and per call replayed from a CUDA graph.
+    Returns a dict of components."""
+    import numpy as np
     import torch
 
     from exact_attention_52_gb300 import api
     from exact_attention_52_gb300.inputs import make_inputs_gqa
 
-    w = EXTRA_WORKLOADS[args.workload]
+    w = EXTRA_WORKLOADS[name]
     B, H, Hk, N, D, causal = w["B"], w["H"], w["Hk"], w["N"], w["d"], w["causal"]
-    torch.cuda.set_device(0)
     inp = make_inputs_gqa(B, H, Hk, N, D, seed=0, with_grad=True)
-    import numpy as np
 
     def dev(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()
@@ -542,61 +691,83 @@ def run_extra(args):
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws = torch.empty(api.bwd_workspace_bytes(B, H, N, D), dtype=torch.uint8, device="cuda")
     stream = torch.cuda.current_stream()
-
+    flush = torch.empty(flush_bytes, dtype=torch.uint8, device="cuda")
     window = w.get("window")
+    ws_split = None
     if w.get("splitkv"):
         ws_split = torch.empty(api.load_library().attn_fwd_splitkv_workspace_bytes(B, H, N, D, 0),
                                dtype=torch.uint8, device="cuda")
 
-    def step(ev=None):
-        if ev:
-            ev[0].record(stream)
+    def fwd_call():
         if window is not None:
             api.fwd_window(q, k, v, *window, o=o, lse=lse)
-        elif w.get("splitkv"):
+        elif ws_split is not None:
             api.fwd_splitkv(q, k, v, num_splits=0, causal=causal, o=o, lse=lse, workspace=ws_split)
         else:
             api.fwd(q, k, v, causal=causal, o=o, lse=lse)
-        if ev:
-            ev[1].record(stream)
+
+    def second_call():
         if w.get("fwd_only"):
-            pass
-        elif window is not None:
+            return
+        if window is not None:
             api.bwd_window(q, k, v, o, do, lse, *window, dq=dq, dk=dk, dv=dv, workspace=ws)
-        elif w.get("splitkv"):
+        elif ws_split is not None:
             api.fwd(q, k, v, causal=causal, o=o, lse=lse)  # single-pass forward, for comparison
         else:
             api.bwd(q, k, v, o, do, lse, causal=causal, dq=dq, dk=dk, dv=dv, workspace=ws)
-        if ev:
-            ev[2].record(stream)
 
-    for _ in range(max(args.warmup, 3)):
-        step()
+    for _ in range(3):
+        fwd_call()
+        second_call()
+    torch.cuda.synchronize()
+    t_f, t_s = [], []
+    for _ in range(steps):
+        flush.zero_()
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        fwd_call()
+        e[1].record(stream)
+        if not w.get("fwd_only"):
+            flush.zero_()
+            e[2].record(stream)
+            second_call()
+            e[3].record(stream)
+        torch.cuda.synchronize()
+        t_f.append(e[0].elapsed_time(e[1]))
+        if not w.get("fwd_only"):
+            t_s.append(e[2].elapsed_time(e[3]))
     rc, site = api.check_device_error()
     if rc != 0:
         raise RuntimeError(f"device error {rc} at wait site {site:#x}")
-    steps = min(args.steps, 50)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    torch.cuda.synchronize()
-    for i in range(steps):
-        step(evs[i])
-    torch.cuda.synchronize()
-    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / steps
-    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / steps
+    fwd_ms = statistics.median(t_f)
     f = attn_flops(B, H, N, D, causal)
     if window is not None:
         f = B * H * window_flops(N, D, *window)
     peaks, kind = load_peaks()
     burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tf = f / (fwd_ms * 1e-3) / 1e12
+    comp = {"fwd": {"ms": round(fwd_ms, 5), "tflops": round(tf, 1),
+                    "frac_of_burst": round(tf / burst, 4)}}
     if w.get("fwd_only"):
         nbytes = attn_bytes(B, H, N, D, "fwd")
-        # The same calls captured in a CUDA graph and replayed: device time per call
-        # without the host-side launch path (argument checks, tensor-map encoding).
+        comp["fwd"]["us"] = round(fwd_ms * 1e3, 2)
+        comp["fwd"]["gbs"] = round(nbytes / (fwd_ms * 1e-3) / 1e9, 1)
+        comp["fwd"]["frac_of_hbm"] = round(nbytes / (fwd_ms * 1e-3) / 1e9 /
+                                           float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"])), 4)
+        # back to back (host path included) and replayed from a CUDA graph (inputs in L2)
+        n_bb = 50
+        b0, b1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        b0.record(stream)
+        for _ in range(n_bb):
+            fwd_call()
+        b1.record(stream)
+        torch.cuda.synchronize()
+        comp["fwd_back_to_back"] = {"us": round(b0.elapsed_time(b1) / n_bb * 1e3, 2), "calls": n_bb}
         per_graph, replays = 20, 50
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             for _ in range(per_graph):
-                step()
+                fwd_call()
         graph.replay()
         torch.cuda.synchronize()
         g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -609,40 +780,35 @@ def run_extra(args):
         if rc != 0:
             raise RuntimeError(f"device error {rc} at wait site {site:#x}")
         graph_ms = g0.elapsed_time(g1) / (replays * per_graph)
-        line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
-                "unit": "TFLOP/s", "value": round(f / (fwd_ms * 1e-3) / 1e12, 3),
-                "components": {"fwd": {"us": round(fwd_ms * 1e3, 2),
-                                       "tflops": round(f / (fwd_ms * 1e-3) / 1e12, 3),
-                                       "gbs": round(nbytes / (fwd_ms * 1e-3) / 1e9, 1),
-                                       "frac_of_burst": round(f / (fwd_ms * 1e-3) / 1e12 / burst, 4)},
-                               "fwd_graph_replay": {"us": round(graph_ms * 1e3, 2),
-                                                    "tflops": round(f / (graph_ms * 1e-3) / 1e12, 3),
-                                                    "gbs": round(nbytes / (graph_ms * 1e-3) / 1e9, 1),
-                                                    "calls_per_graph": per_graph,
-                                                    "replays": replays}},
-                "note": "fwd: time per call between CUDA events, host-side argument checks and "
-                        "tensor-map encoding included; fwd_graph_replay: the same calls "
-                        "replayed from a CUDA graph (inputs stay in L2 between calls)",
-                "peak_kind": kind, "dtype": "bf16", "data": "synthetic"}
-        print(json.dumps(line), flush=True)
-        return 0
-    if w.get("splitkv"):
-        line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
-                "unit": "TFLOP/s", "value": round(f / (fwd_ms * 1e-3) / 1e12, 2),
-                "components": {
-                    "fwd_splitkv": {"ms": round(fwd_ms, 4), "tflops": round(f / (fwd_ms * 1e-3) / 1e12, 1)},
-                    "fwd_single_pass": {"ms": round(bwd_ms, 4),
-                                        "tflops": round(f / (bwd_ms * 1e-3) / 1e12, 1)}},
-                "dtype": "bf16", "data": "synthetic"}
-        print(json.dumps(line), flush=True)
-        return 0
-    line = {"metric": METRIC, "workload": args.workload, "config": w, "steps": steps,
-            "value": round(3.5 * f / ((fwd_ms + bwd_ms) * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-            "components": {
-                "fwd": {"ms": round(fwd_ms, 4), "tflops": round(f / (fwd_ms * 1e-3) / 1e12, 1),
-                        "frac_of_burst": round(f / (fwd_ms * 1e-3) / 1e12 / burst, 4)},
-                "bwd": {"ms": round(bwd_ms, 4), "tflops": round(2.5 * f / (bwd_ms * 1e-3) / 1e12, 1),
-                        "frac_of_burst": round(2.5 * f / (bwd_ms * 1e-3) / 1e12 / burst, 4)}},
+        comp["fwd_graph_replay"] = {"us": round(graph_ms * 1e3, 2),
+                                    "tflops": round(f / (graph_ms * 1e-3) / 1e12, 1),
+                                    "gbs": round(nbytes / (graph_ms * 1e-3) / 1e9, 1),
+                                    "calls_per_graph": per_graph, "replays": replays}
+    elif ws_split is not None:
+        s_ms = statistics.median(t_s)
+        comp = {"fwd_splitkv": comp["fwd"],
+                "fwd_single_pass": {"ms": round(s_ms, 5), "tflops": round(f / (s_ms * 1e-3) / 1e12, 1)}}
+    else:
+        b_ms = statistics.median(t_s)
+        tb = 2.5 * f / (b_ms * 1e-3) / 1e12
+        comp["bwd"] = {"ms": round(b_ms, 5), "tflops": round(tb, 1), "frac_of_burst": round(tb / burst, 4)}
+    del flush
+    torch.cuda.empty_cache()
+    return comp, f, kind
+
+
+def run_extra(args):
+    """Forward (+ backward) on one of EXTRA_WORKLOADS: a secondary line; the
+    default run measures the benchmark step."""
+    import torch
+    torch.cuda.set_device(0)
+    comp, f, kind = measure_workload(args.workload, steps=min(args.steps, 50))
+    main_ms = comp.get("fwd", comp.get("fwd_splitkv"))["ms"] + comp.get("bwd", {}).get("ms", 0.0)
+    mult = 3.5 if "bwd" in comp else 1.0
+    line = {"metric": METRIC, "workload": args.workload, "config": EXTRA_WORKLOADS[args.workload],
+            "steps": min(args.steps, 50), "unit": "TFLOP/s",
+            "value": round(mult * f / (main_ms * 1e-3) / 1e12, 2), "components": comp,
+            "timing": "median device time per call between CUDA events, L2 flushed before each call",
             "peak_kind": kind, "dtype": "bf16", "data": "synthetic"}
     print(json.dumps(line), flush=True)
     return 0
@@ -657,6 +823,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (used for profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the small-configuration lines (C1-C3) after the timed region")
+    ap.add_argument("--no-live-peaks", action="store_true",
+                    help="skip the live cuBLAS GEMM peaks (FP8 roofline denominator)")
     ap.add_argument("--workload", choices=("main",) + tuple(EXTRA_WORKLOADS), default="main",
                     help="secondary workloads print their own line (not the benchmark step)")
     args = ap.parse_args()

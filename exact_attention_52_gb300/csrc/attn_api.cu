@@ -23,42 +23,50 @@ unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
 
 constexpr int kMaxDevices = 64;
 
-struct DeviceState {
+// Architecture check, cached per device (a device's compute capability never
+// changes).
+struct DeviceArch {
     bool probed = false;
     bool supported = false;
-    unsigned int* err = nullptr;  // device address of g_err_word on this device
 };
-DeviceState g_dev[kMaxDevices];
+DeviceArch g_dev[kMaxDevices];
 std::mutex g_dev_mutex;
 
-// Per-device setup, done once with that device current: check the
-// architecture and look up the device address of the error word.
-attn_status device_state(DeviceState** out) {
+// Current device: check the architecture and look up the device address of the
+// error word.  The address is looked up on every call, not cached: it belongs
+// to the module loaded into the device's current context, and a context made
+// after cudaDeviceReset (or another context made current on the same device)
+// loads the module again, possibly at another address.  The lookup allocates
+// nothing.
+struct DeviceState {
+    unsigned int* err = nullptr;  // device address of g_err_word in the current context
+};
+
+attn_status device_state(DeviceState* out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_dev_mutex);
-    DeviceState& s = g_dev[dev];
-    if (!s.probed) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        s.supported = (major == 10 && minor == 3);
-        void* p = nullptr;
-        if (s.supported) {
-            if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return ATTN_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(g_dev_mutex);
+        DeviceArch& a = g_dev[dev];
+        if (!a.probed) {
+            int major = 0, minor = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            a.supported = (major == 10 && minor == 3);
+            a.probed = true;
         }
-        s.err = static_cast<unsigned int*>(p);
-        s.probed = true;
+        if (!a.supported) return ATTN_ERR_UNSUPPORTED;
     }
-    if (!s.supported) return ATTN_ERR_UNSUPPORTED;
-    *out = &s;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    out->err = static_cast<unsigned int*>(p);
     return ATTN_OK;
 }
 
-DevStatus dev_status(const DeviceState* s) {
+DevStatus dev_status(const DeviceState& s) {
     DevStatus st;
-    st.word = s->err;
+    st.word = s.err;
     st.wait_limit_ns = g_wait_limit_ns;
     return st;
 }
@@ -222,7 +230,7 @@ attn_status fwd_run(const void* q, const Strides& qs, const void* k, const Strid
         return ATTN_ERR_INVALID;
     if (!strides_ok(qs, 2) || !strides_ok(ks, 2) || !strides_ok(vs, 2) || !strides_ok(os, 2))
         return ATTN_ERR_INVALID;
-    DeviceState* ds = nullptr;
+    DeviceState ds;
     if ((rc = device_state(&ds)) != ATTN_OK) return rc;
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, q, false, d, N, H, B, qs) || !make_map(&tk, k, false, d, N, Hk, B, ks) ||
@@ -273,7 +281,7 @@ size_t splitkv_bytes(int B, int H, int N, int d, int S) {
 
 // Validated view of the backward workspace.
 struct BwdCall {
-    DeviceState* ds = nullptr;
+    DeviceState ds;
     float* dq_acc = nullptr;
     float* lse2 = nullptr;
     float* dsum = nullptr;
@@ -428,6 +436,10 @@ Strides from_abi(const attn_strides_t& s) {
 
 }  // namespace
 
+int check_problem(int B, int H, int N, int d, float scale, int causal) {
+    return static_cast<int>(check_sizes(B, H, N, d, scale, causal));
+}
+
 cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream) {
     wait_selftest_kernel<<<1, 64, 0, stream>>>(st);
     return cudaGetLastError();
@@ -490,9 +502,10 @@ attn_status attn_fwd_splitkv(const void* q, const void* k, const void* v, void* 
     const int n_kv = (N + kTile - 1) / kTile;
     int S = num_splits;
     if (S == 0) {
-        int dev = 0, sms = 148;
-        if (cudaGetDevice(&dev) == cudaSuccess)
-            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
         S = auto_splits(BH, N, sms);
     }
     if (S > n_kv) S = n_kv;
@@ -536,7 +549,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
         if (!(s > 0.f) || !std::isfinite(s)) return ATTN_ERR_INVALID;
     if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
         return ATTN_ERR_INVALID;
-    DeviceState* ds = nullptr;
+    DeviceState ds;
     if ((rc = device_state(&ds)) != ATTN_OK) return rc;
     const Strides st = dense(H, N, d);
     CUtensorMap tq, tk, tv;
@@ -641,15 +654,15 @@ attn_status attn_bwd_strided(const void* q, attn_strides_t qs, const void* k, at
 
 attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site) {
     if (site) *site = 0;
-    DeviceState* ds = nullptr;
+    DeviceState ds;
     attn_status rc = device_state(&ds);
     if (rc != ATTN_OK) return rc;
     if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return ATTN_ERR_CUDA;
     unsigned int host[2] = {0, 0};
     const unsigned int zero[2] = {0, 0};
-    if (cudaMemcpy(host, ds->err, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess ||
-        cudaMemcpy(ds->err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    if (cudaMemcpy(host, ds.err, sizeof(host), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(ds.err, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return ATTN_ERR_CUDA;
     if (site) *site = host[1];
     return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
@@ -660,7 +673,7 @@ void attn_set_wait_limit_ns(unsigned long long ns) {
 }
 
 attn_status attn_selftest_wait_timeout(attn_stream_t stream) {
-    DeviceState* ds = nullptr;
+    DeviceState ds;
     attn_status rc = device_state(&ds);
     if (rc != ATTN_OK) return rc;
     return launch_wait_selftest(dev_status(ds), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

@@ -767,9 +767,17 @@ cudaError_t launch_fwd_fp8(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 }
 
 cudaError_t launch_splitkv_combine(const CombineParams& p, cudaStream_t stream) {
+    // One warp per row, eight rows per block; at most 16 blocks per SM (of the
+    // device the launch goes to), the warps striding over the remaining rows.
     const long long rows = static_cast<long long>(p.BH) * p.N;
     const long long blocks = (rows + 7) / 8;
-    const int grid = static_cast<int>(blocks < 152 * 16 ? blocks : 152 * 16);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const long long cap = 16ll * sms;
+    const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+    if (grid < 1) return cudaSuccess;
     splitkv_combine_kernel<<<grid, 256, 0, stream>>>(p);
     return cudaGetLastError();
 }

@@ -99,6 +99,10 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream);
 cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream);
 
+// Problem check shared by the entry points (sizes, head dim, scale, causal
+// flag); returns an attn_status value (0 = valid).
+int check_problem(int B, int H, int N, int d, float scale, int causal);
+
 // Shared-memory bytes a launcher requests (for tests of the host logic).
 int fwd_smem_bytes(int D, bool fp8);
 int bwd_smem_bytes(int D);

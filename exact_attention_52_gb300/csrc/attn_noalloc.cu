@@ -21,6 +21,7 @@
 #include <cstddef>
 #include <mutex>
 
+#include "attn_internal.h"
 #include "attn_sm103a.h"
 
 namespace {
@@ -30,34 +31,39 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[kNoAllocScratchBytes];
 
-struct ScratchState {
-    bool ready = false;
-    void* ptr = nullptr;  // device address of g_bwd_scratch on that device
-};
-ScratchState g_scratch[kMaxDevices];
-std::mutex g_scratch_mutex;
+// Architecture check, cached per device (a device's compute capability never
+// changes).
+bool g_arch_checked[kMaxDevices];
+bool g_arch_ok[kMaxDevices];
+std::mutex g_arch_mutex;
 
-// Once per device, with that device current: check the architecture and look
-// up the device address of the scratch array.  In host code the array's name
-// is only a host-side stand-in, never a usable device pointer.
+// The scratch array's device address on the current device.  In host code the
+// array's name is only a host-side stand-in, never a usable device pointer, so
+// the address is looked up with that device current.  It is looked up on every
+// call rather than cached: the address belongs to the module loaded into the
+// device's current context, and a context created after cudaDeviceReset (or a
+// different context made current on the same device) loads the module again,
+// possibly elsewhere.  The lookup allocates nothing.  On the first call in a
+// context it may load the library's module into that context, which is why the
+// first call should come before any stream capture.
 attn_status scratch_for_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    ScratchState& s = g_scratch[dev];
-    if (!s.ready) {
-        int major = 0, minor = 0;
-        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-            return ATTN_ERR_CUDA;
-        if (!(major == 10 && minor == 3)) return ATTN_ERR_UNSUPPORTED;
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr)
-            return ATTN_ERR_CUDA;
-        s.ptr = p;
-        s.ready = true;
+    {
+        std::lock_guard<std::mutex> lock(g_arch_mutex);
+        if (!g_arch_checked[dev]) {
+            int major = 0, minor = 0;
+            if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+                return ATTN_ERR_CUDA;
+            g_arch_ok[dev] = (major == 10 && minor == 3);
+            g_arch_checked[dev] = true;
+        }
+        if (!g_arch_ok[dev]) return ATTN_ERR_UNSUPPORTED;
     }
-    *out = s.ptr;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || p == nullptr) return ATTN_ERR_CUDA;
+    *out = p;
     return ATTN_OK;
 }
 
@@ -67,6 +73,11 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
                                         const void* dout, const float* lse, void* dq, void* dk,
                                         void* dv, int B, int H, int N, int d, float scale,
                                         int causal, attn_stream_t stream) {
+    // The problem is checked the way attn_bwd checks it (same status for a bad
+    // size, head dim or flag) before the scratch limit is applied.
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    const attn_status chk = static_cast<attn_status>(attn::check_problem(B, H, N, d, scale, causal));
+    if (chk != ATTN_OK) return chk;
     const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
     if (need == 0) return ATTN_ERR_INVALID;
     if (need > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;

@@ -130,15 +130,21 @@ attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, 
  * input and output tensors while the framework owns all device memory and
  * allows no allocation after start-up.  The pages describe no such variant;
  * it has no counterpart there.
- *   Arguments, results and errors are those of attn_bwd, with the scratch
- *   taken from a fixed 64 MiB array inside the library instead of
- *   `workspace`.  Problems whose attn_bwd_workspace_bytes() exceeds 64 MiB
- *   are rejected with ATTN_ERR_UNSUPPORTED before anything is launched
- *   (about 129k padded rows at d = 128, e.g. B*H*ceil(N/128)*128 <= 129,000).
- *   The first call on a device looks up the array's device address once
- *   (with that device current); make that first call before any stream
- *   capture.  Every GPU that loads this part of the library keeps the 64 MiB
- *   until the process exits.  Nothing is allocated by any call.
+ *   Arguments and results are those of attn_bwd, with the scratch taken
+ *   from a fixed 64 MiB array inside the library instead of `workspace`.
+ *   The problem is checked first, as attn_bwd checks it, with the same
+ *   status (ATTN_ERR_INVALID for bad sizes, scale or flag,
+ *   ATTN_ERR_UNSUPPORTED for a head dim other than 64 or 128); a valid
+ *   problem whose attn_bwd_workspace_bytes() exceeds 64 MiB is then rejected
+ *   with ATTN_ERR_UNSUPPORTED, before anything is launched (about 129k padded
+ *   rows at d = 128, e.g. B*H*ceil(N/128)*128 <= 129,000).  Pointer and
+ *   launch errors are those of attn_bwd.
+ *   Every call looks up the array's device address in the current context
+ *   (a lookup, no allocation), so the entry point stays valid after
+ *   cudaDeviceReset or a change of context.  The first call in a context may
+ *   load the library's device code into it: make that first call before any
+ *   stream capture.  Every GPU that loads this part of the library keeps the
+ *   64 MiB until the process exits.  Nothing is allocated by any call.
  *   All calls on a device share the one array: calls that overlap on the GPU
  *   (unordered streams) race and give wrong results.  Each call zeroes the
  *   part that must start at zero, so earlier calls do not leak into later ones.

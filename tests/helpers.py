@@ -44,6 +44,23 @@ def rel_fro(a, b):
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
 
 
+def grad_rel_err(gpu, ref, tile=128):
+    """Largest relative Frobenius error of a gradient over the whole tensor and
+    over every block of ``tile`` consecutive rows (second-to-last axis) of
+    every head: a single wrong row, ragged tail or mis-indexed tile moves its
+    own block's error by O(1) even where the whole-tensor figure hides it."""
+    gpu = np.asarray(gpu, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    worst = rel_fro(gpu, ref)
+    n = ref.shape[-2] if ref.ndim >= 2 else ref.shape[0]
+    g2 = gpu.reshape((-1,) + gpu.shape[-2:]) if gpu.ndim >= 2 else gpu.reshape(1, -1, 1)
+    r2 = ref.reshape((-1,) + ref.shape[-2:]) if ref.ndim >= 2 else ref.reshape(1, -1, 1)
+    for i in range(r2.shape[0]):
+        for t0 in range(0, n, tile):
+            worst = max(worst, rel_fro(g2[i, t0:t0 + tile], r2[i, t0:t0 + tile]))
+    return worst
+
+
 def bf16_to_device(bits):
     import torch
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).cuda()

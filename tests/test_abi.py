@@ -106,3 +106,19 @@ def test_invalid_arguments_are_rejected_before_launch(lib):
 def test_binding_raises_when_library_missing(tmp_path):
     with pytest.raises(RuntimeError, match="not built"):
         api.load_library(str(tmp_path / "libattn_sm103a.so"))
+
+
+def test_noalloc_checks_the_problem_before_its_scratch_limit(lib):
+    """attn_bwd_noalloc gives attn_bwd's status for a bad problem, and rejects a
+    valid one that needs more than its 64 MiB scratch, before touching the
+    device (no GPU here: any device call would fail with ATTN_ERR_CUDA)."""
+    fake = ctypes.c_void_p(1 << 20)
+    args = [fake] * 9
+    INVALID, UNSUP = -1, -2
+    assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 96, 0.1, 0, None) == UNSUP
+    assert lib.attn_bwd_noalloc(*args, 0, 1, 128, 128, 0.1, 0, None) == INVALID
+    assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 128, 0.1, 2, None) == INVALID
+    assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 128, float("inf"), 0, None) == INVALID
+    assert lib.attn_bwd_noalloc(*args, 1, 32, 8192, 128, 0.088, 0, None) == UNSUP
+    assert lib.attn_bwd_workspace_bytes(1, 15, 8192, 128) <= 64 << 20 < lib.attn_bwd_workspace_bytes(
+        1, 32, 8192, 128)

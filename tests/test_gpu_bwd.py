@@ -8,7 +8,8 @@ import oracle
 from exact_attention_52_gb300 import api
 from exact_attention_52_gb300.inputs import make_inputs
 
-from .helpers import TOL_GRAD_RELFRO, bf16_to_device, decoded, device_bf16_to_f64, rel_fro
+from .helpers import (TOL_GRAD_RELFRO, bf16_to_device, decoded, device_bf16_to_f64, grad_rel_err,
+                      rel_fro)
 
 pytestmark = pytest.mark.gpu
 
@@ -32,7 +33,7 @@ def test_bwd_matches_oracle(N, d, causal):
     ref = oracle.backward(q, k, v, do, 1.0 / np.sqrt(d), causal)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
         assert np.all(np.isfinite(g)), name
-        err = rel_fro(g, r)
+        err = grad_rel_err(g, r)
         assert err <= TOL_GRAD_RELFRO, (name, err)
 
 
@@ -42,7 +43,7 @@ def test_bwd_batches_heads_outliers():
     q, k, v, do = decoded(inp)
     ref = oracle.backward(q, k, v, do, 1.0 / np.sqrt(128), False)
     for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-        assert rel_fro(g, r) <= TOL_GRAD_RELFRO, name
+        assert grad_rel_err(g, r) <= TOL_GRAD_RELFRO, name
 
 
 def test_bwd_dk_dv_deterministic_dq_within_tolerance():

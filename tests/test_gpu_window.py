@@ -11,7 +11,7 @@ from exact_attention_52_gb300 import api
 from exact_attention_52_gb300.inputs import make_inputs_gqa
 
 from .helpers import (TOL_GRAD_RELFRO, TOL_LSE_ABS, TOL_O_MAXABS, bf16_out_err, bf16_to_device,
-                      decoded, device_bf16_to_f64, device_f32_to_f64, max_abs, rel_fro)
+                      decoded, device_bf16_to_f64, device_f32_to_f64, max_abs, grad_rel_err)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +34,7 @@ def test_window_fwd_bwd_match_oracle(window, N, H, Hk, d):
     assert max_abs(device_f32_to_f64(lse), lse_ref) <= TOL_LSE_ABS
     ref = oracle.backward_gqa(qf, kf, vf, dof, scale, False, window=window)
     for name, g, r in zip(("dq", "dk", "dv"), (dq, dk, dv), ref):
-        err = rel_fro(device_bf16_to_f64(g), r)
+        err = grad_rel_err(device_bf16_to_f64(g), r)
         assert err <= TOL_GRAD_RELFRO, (name, err)
 
 

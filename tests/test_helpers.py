@@ -23,3 +23,18 @@ def test_metrics():
     a = np.array([1.0, 2.0, 3.0])
     assert max_abs(a, a + [0, 0.5, 0]) == 0.5
     assert rel_fro(a * 1.01, a) == pytest.approx(0.01)
+
+
+def test_grad_rel_err_catches_one_wrong_row():
+    from .helpers import grad_rel_err
+    rng = np.random.Generator(np.random.PCG64(1))
+    ref = rng.standard_normal((2, 8192, 128))
+    gpu = ref * (1 + 1e-3 * rng.standard_normal(ref.shape))
+    assert grad_rel_err(gpu, ref) < 2e-3
+    bad = gpu.copy()
+    bad[1, 5000] = 0.0  # one row lost
+    assert rel_fro(bad, ref) < 2e-2  # the whole-tensor figure alone would pass
+    assert grad_rel_err(bad, ref) > 0.05  # its 128-row block does not
+    tail = gpu[:, :8000].copy()
+    tail[0, -3:] *= -1.0  # a ragged last block with a sign error
+    assert grad_rel_err(tail, ref[:, :8000]) > 0.1

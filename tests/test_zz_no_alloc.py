@@ -3,22 +3,33 @@ memory (code handed only its input and output tensors by a framework that owns
 all device memory).  It runs on a fixed scratch array inside the library.
 
 Checked through the C ABI against attn_bwd (which takes a caller-allocated
-workspace) on two calls in a row with different inputs, so that anything left
-in the shared scratch by the first call would show up in the second.  This
-file is collected last so that a failure here cannot hide other tests; it also
-passes when run alone in a fresh process."""
+workspace) on three calls in a row with different inputs and sizes -- a small
+one, one that uses nearly all of the 64 MiB scratch, then a small one again --
+so that anything left in the shared scratch by an earlier call would show up
+in a later one:
+  * dK and dV come from the same deterministic kernels and must be
+    bit-identical to attn_bwd's;
+  * dQ is summed by fp32 reductions in an order that may differ between the
+    two calls, so it is compared within the rounding of its bf16 output;
+  * all three gradients are also compared with the fp64 oracle.
+This file is collected last so that a failure here cannot hide other tests; it
+also passes when run alone in a fresh process."""
 
 import ctypes
 
 import numpy as np
 import pytest
 
+import oracle
 from exact_attention_52_gb300 import api
 from exact_attention_52_gb300.inputs import make_inputs
 
-from .helpers import TOL_GRAD_RELFRO, bf16_to_device, device_bf16_to_f64, rel_fro
+from .helpers import (TOL_GRAD_RELFRO, bf16_to_device, decoded, device_bf16_to_f64, grad_rel_err,
+                      rel_fro)
 
 pytestmark = pytest.mark.gpu
+
+SCRATCH_BYTES = 64 << 20
 
 
 def _call_noalloc(lib, q, k, v, o, do, lse, causal):
@@ -33,25 +44,49 @@ def _call_noalloc(lib, q, k, v, o, do, lse, causal):
     return dq, dk, dv
 
 
+# (B, H, N, d, oracle heads): the middle call needs 61 MiB of scratch
+CALLS = [(1, 3, 700, 128, None), (1, 15, 8192, 128, [(0, 7)]), (2, 2, 513, 64, None)]
+
+
 @pytest.mark.parametrize("causal", [False, True])
-def test_noalloc_matches_workspace_backward_twice(causal):
+def test_noalloc_matches_workspace_backward_three_calls(causal):
     lib = api.load_library()
-    for call, (B, H, N, d) in enumerate([(1, 3, 700, 128), (2, 2, 513, 64)]):
-        inp = make_inputs(B, H, N, d, seed=40 + call, with_grad=True)
+    for call, (B, H, N, d, heads) in enumerate(CALLS):
+        assert lib.attn_bwd_workspace_bytes(B, H, N, d) <= SCRATCH_BYTES
+        inp = make_inputs(B, H, N, d, seed=40 + call + 10 * int(causal), with_grad=True)
         q, k, v, do = (bf16_to_device(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
         o, lse = api.fwd(q, k, v, causal=causal)
         ref = api.bwd(q, k, v, o, do, lse, causal=causal)
         got = _call_noalloc(lib, q, k, v, o, do, lse, causal)
         rc, site = api.check_device_error()
         assert rc == 0, f"device error {rc} at site {site:#x}"
-        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
-            err = rel_fro(device_bf16_to_f64(g), device_bf16_to_f64(r))
-            assert err <= TOL_GRAD_RELFRO, (call, name, err)
+        dq_g, dk_g, dv_g = (device_bf16_to_f64(t) for t in got)
+        dq_r, dk_r, dv_r = (device_bf16_to_f64(t) for t in ref)
+        assert np.array_equal(dk_g, dk_r), (call, "dk")
+        assert np.array_equal(dv_g, dv_r), (call, "dv")
+        assert rel_fro(dq_g, dq_r) <= 1e-4, (call, rel_fro(dq_g, dq_r))
+        qd, kd, vd, dod = decoded(inp)
+        scale = 1.0 / np.sqrt(d)
+        if heads is None:
+            refs = oracle.backward(qd, kd, vd, dod, scale, causal)
+            for name, g, r in zip(("dq", "dk", "dv"), (dq_g, dk_g, dv_g), refs):
+                assert grad_rel_err(g, r) <= TOL_GRAD_RELFRO, (call, name)
+        else:
+            for (b, h) in heads:
+                refs = oracle.head_backward(qd[b, h], kd[b, h], vd[b, h], dod[b, h], scale, causal)
+                for name, g, r in zip(("dq", "dk", "dv"), (dq_g, dk_g, dv_g), refs[:3]):
+                    assert grad_rel_err(g[b, h], r) <= TOL_GRAD_RELFRO, (call, name, b, h)
 
 
 def test_noalloc_rejects_problems_larger_than_its_scratch():
     lib = api.load_library()
-    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size checks come first
     args = [fake] * 9
     # B*H*Npad*d*4 bytes for the fp32 accumulator alone exceeds 64 MiB here
     assert lib.attn_bwd_noalloc(*args, 1, 32, 8192, 128, 0.088, 0, None) == -2
+    # an unsupported head dim gets attn_bwd's own status, before the size limit
+    assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 96, 0.1, 0, None) == -2
+    # invalid sizes and flags: ATTN_ERR_INVALID, as attn_bwd
+    assert lib.attn_bwd_noalloc(*args, 0, 1, 128, 128, 0.1, 0, None) == -1
+    assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 128, 0.1, 2, None) == -1
+    assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 128, -1.0, 0, None) == -1
