@@ -169,6 +169,19 @@ __global__ void __launch_bounds__(320, 1)
         return w;
     };
 
+    // The r-th item of this CTA.  Round r holds items [r G, r G + G); even rounds
+    // are dealt in CTA order and odd rounds in reverse (a snake), so that with
+    // items in longest-first order (causal) the CTAs' totals stay within about
+    // one item of each other, as the hardware block scheduler's would, while the
+    // CTAs stay resident.  Returns -1 after the last round and -2 for a round in
+    // which this CTA has no item (only the last one can be short).
+    auto item_at = [&](int r) -> int {
+        const long long base = static_cast<long long>(r) * gridDim.x;
+        if (base >= n_items) return -1;
+        const int c = (r & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+        return base + c < n_items ? static_cast<int>(base + c) : -2;
+    };
+
     if (threadIdx.x == 0) {
         mbar_init(b_q, 1);
         for (int s = 0; s < T::KV_SLOTS; ++s) {
@@ -205,7 +218,10 @@ __global__ void __launch_bounds__(320, 1)
             int idx = 0;  // K/V loads issued so far (ring position), over all items
             int k = 0;    // items started
             bool ok = true;
-            for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++k) {
+            for (int r = 0; ok; ++r) {
+                const int item = item_at(r);
+                if (item == -1) break;
+                if (item < 0) continue;
                 const Item it = item_info(item);
                 // K_j, V_j of the item's key tile j into the ring
                 auto load_kv = [&](int j) -> bool {
@@ -243,6 +259,7 @@ __global__ void __launch_bounds__(320, 1)
                                     blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile, it.h_idx, it.b_idx);
                 }
                 for (int j = 1; j < it.n_kv && ok; ++j) ok = load_kv(j);
+                ++k;
             }
             // Let every copy this thread started land before the CTA can exit.
             if (k > 0) wait_drain(b_q, (k - 1) & 1, prm.st, SITE_DRAIN);
@@ -432,8 +449,11 @@ __global__ void __launch_bounds__(320, 1)
                 }
                 return true;
             };
-            int k = 0;
-            for (int item = blockIdx.x; item < n_items; item += gridDim.x, ++k) {
+            int k = 0;  // items issued
+            for (int r = 0;; ++r) {
+                const int item = item_at(r);
+                if (item == -1) break;
+                if (item < 0) continue;
                 it = item_info(item);
                 q_released = false;
                 if (!wait_warp(b_q, k & 1, abort_flag, prm.st, SITE_Q)) break;
@@ -448,6 +468,7 @@ __global__ void __launch_bounds__(320, 1)
                 ring += 2 * it.n_kv;
                 pdone0 += it.n0;
                 pdone1 += it.n1;
+                ++k;
             }
             // Every MMA issued above must finish before tensor memory is freed.
             mma_commit_warp(b_done);
@@ -466,7 +487,10 @@ __global__ void __launch_bounds__(320, 1)
         int s_seen = 0;  // S tiles of this query tile consumed in earlier items
         int o_seen = 0;  // outputs of this query tile written in earlier items
         bool ok = true;
-        for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        for (int r = 0; ok; ++r) {
+        const int item = item_at(r);
+        if (item == -1) break;
+        if (item < 0) continue;
         const Item it = item_info(item);
         const int bh = it.bh, split = it.split, b_idx = it.b_idx, h_idx = it.h_idx;
         const int q_row = (2 * it.pair + g) * kTile + row;
@@ -733,13 +757,12 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     static const cudaError_t attr = cudaFuncSetAttribute(
         fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
-    // Items of equal size (no causal mask): persistent CTAs, one per SM (shared memory
-    // admits one), each looping over items.  Causal items differ in size, and the
-    // hardware's block scheduler handing the longest-first items to whichever SM frees
-    // up balances them better than a fixed assignment: one item per CTA there.
+    // Persistent CTAs, one per SM (shared memory admits one), each looping over
+    // items in the snake order of item_at: equal items (no mask) and longest-first
+    // causal items alike end within about one item of each other.
     const long long items = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
     long long grid = items;
-    if (p.causal == 0) {
+    {
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

@@ -44,10 +44,21 @@ def rel_fro(a, b):
     return float(np.linalg.norm(a - b) / den) if den > 0 else float(np.linalg.norm(a - b))
 
 
+def row_blocks(n, tile=128):
+    """[start, stop) blocks of ``tile`` rows covering n rows; a ragged last block
+    shorter than tile / 2 is merged into the block before it, so that no block
+    is so short that the output's own rounding noise decides its error (one row
+    with two visible keys can be 3 % off its own norm from bf16 rounding)."""
+    starts = list(range(0, n, tile))
+    if len(starts) > 1 and n - starts[-1] < tile // 2:
+        starts.pop()
+    return [(a, starts[i + 1] if i + 1 < len(starts) else n) for i, a in enumerate(starts)]
+
+
 def grad_rel_err(gpu, ref, tile=128):
     """Largest relative Frobenius error of a gradient over the whole tensor and
-    over every block of ``tile`` consecutive rows (second-to-last axis) of
-    every head: a single wrong row, ragged tail or mis-indexed tile moves its
+    over every block of about ``tile`` consecutive rows (second-to-last axis)
+    of every head: a single wrong row, ragged tail or mis-indexed tile moves its
     own block's error by O(1) even where the whole-tensor figure hides it."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
@@ -56,8 +67,8 @@ def grad_rel_err(gpu, ref, tile=128):
     g2 = gpu.reshape((-1,) + gpu.shape[-2:]) if gpu.ndim >= 2 else gpu.reshape(1, -1, 1)
     r2 = ref.reshape((-1,) + ref.shape[-2:]) if ref.ndim >= 2 else ref.reshape(1, -1, 1)
     for i in range(r2.shape[0]):
-        for t0 in range(0, n, tile):
-            worst = max(worst, rel_fro(g2[i, t0:t0 + tile], r2[i, t0:t0 + tile]))
+        for a, b in row_blocks(n, tile):
+            worst = max(worst, rel_fro(g2[i, a:b], r2[i, a:b]))
     return worst
 
 

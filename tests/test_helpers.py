@@ -38,3 +38,12 @@ def test_grad_rel_err_catches_one_wrong_row():
     tail = gpu[:, :8000].copy()
     tail[0, -3:] *= -1.0  # a ragged last block with a sign error
     assert grad_rel_err(tail, ref[:, :8000]) > 0.1
+
+
+def test_row_blocks_merge_short_tails():
+    from .helpers import row_blocks
+    assert row_blocks(1) == [(0, 1)]
+    assert row_blocks(128) == [(0, 128)]
+    assert row_blocks(513) == [(0, 128), (128, 256), (256, 384), (384, 513)]
+    assert row_blocks(8000)[-1] == (7936, 8000)  # 64 rows: kept as a block of its own
+    assert row_blocks(300) == [(0, 128), (128, 300)]
