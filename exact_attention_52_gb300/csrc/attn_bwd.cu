@@ -178,6 +178,58 @@ __global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const DqConvert
 }
 
 // ---------------------------------------------------------------------------
+// Work of one backward CTA: one 128-row key tile of one key/value head and the
+// query tiles (of every query head of its group) that see some key of it.
+// ---------------------------------------------------------------------------
+struct BwdWork {
+    int kv_bh, j;        // (batch, key/value head) index and key tile
+    int n_q_total;       // query tiles of a head
+    int q_lo, n_qh;      // query tiles [q_lo, q_lo + n_qh) see this key tile
+    bool full_range;     // every query tile does
+    int q_bh0;           // first query (batch, head) index of the group
+    int b_idx, hk_idx;   // batch, key/value head
+    int bH0;             // (batch, head) index of head 0 of this batch
+    int n_steps;         // G * n_qh
+
+    __device__ explicit BwdWork(const BwdParams& prm) {
+        const int N = prm.N;
+        // Non-causal: head-major order keeps the resident CTAs on a few heads, so
+        // those heads' Q, dO and fp32 dQ accumulator stay in L2 while every key
+        // tile reduces into them.  Causal: low key tiles (longest loops) of every
+        // head first, which keeps the tail of the launch short.
+        kv_bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BHk) : static_cast<int>(blockIdx.x / prm.n_kv);
+        j = prm.causal ? static_cast<int>(blockIdx.x / prm.BHk) : static_cast<int>(blockIdx.x % prm.n_kv);
+        n_q_total = (N + kTile - 1) / kTile;
+        // Query tiles holding the rows that see some key of this tile (window
+        // i - win_left <= key <= i + win_right; negative = no bound).
+        const int kr0 = j * kTile, kr1 = min(N - 1, j * kTile + kTile - 1);
+        const int qrow_lo = prm.win_right < 0 ? 0 : max(0, kr0 - prm.win_right);
+        const int qrow_hi = prm.win_left < 0 ? N - 1 : min(N - 1, kr1 + prm.win_left);
+        q_lo = qrow_lo / kTile;
+        n_qh = qrow_lo <= qrow_hi ? qrow_hi / kTile - q_lo + 1 : 0;  // per query head
+        full_range = (q_lo == 0 && n_qh == n_q_total);
+        // The G query heads sharing this key/value head (G = 1 without grouping)
+        // are visited one after the other; dK and dV accumulate over all of them.
+        const int G = prm.H / prm.Hk;
+        q_bh0 = (kv_bh / prm.Hk) * prm.H + (kv_bh % prm.Hk) * G;
+        b_idx = kv_bh / prm.Hk;
+        hk_idx = kv_bh % prm.Hk;
+        bH0 = b_idx * prm.H;
+        n_steps = G * n_qh;
+    }
+    // Query tile of step t (tt = step index within one query head).  Over the
+    // full range each key tile starts at its own index and wraps, so CTAs that
+    // run together reduce into different dQ tiles; otherwise (causal, windows)
+    // the range is walked upwards, which already starts neighbouring key tiles
+    // on different query tiles.
+    __device__ int q_tile(int tt) const {
+        if (!full_range) return q_lo + tt;
+        const int i = j + tt;
+        return i < n_q_total ? i : i - n_q_total;
+    }
+};
+
+// ---------------------------------------------------------------------------
 // 2. main kernel
 // ---------------------------------------------------------------------------
 // Each 128-row query tile is processed as two 64-row halves h, each with its
@@ -216,39 +268,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 
     const int N = prm.N;
-    // Non-causal: head-major order keeps the resident CTAs on a few heads, so
-    // those heads' Q, dO and fp32 dQ accumulator stay in L2 while every key
-    // tile reduces into them.  Causal: low key tiles (longest loops) of every
-    // head first, which keeps the tail of the launch short.
-    const int kv_bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BHk)
-                                 : static_cast<int>(blockIdx.x / prm.n_kv);
-    const int j = prm.causal ? static_cast<int>(blockIdx.x / prm.BHk)
-                             : static_cast<int>(blockIdx.x % prm.n_kv);  // key tile
-    const int n_q_total = (N + kTile - 1) / kTile;
-    // Query tiles [q_lo, q_lo + n_qh) hold the rows that see some key of this
-    // tile (window i - win_left <= key <= i + win_right; negative = no bound).
-    const int kr0 = j * kTile, kr1 = min(N - 1, j * kTile + kTile - 1);
-    const int qrow_lo = prm.win_right < 0 ? 0 : max(0, kr0 - prm.win_right);
-    const int qrow_hi = prm.win_left < 0 ? N - 1 : min(N - 1, kr1 + prm.win_left);
-    const int q_lo = qrow_lo / kTile;
-    const int n_qh = qrow_lo <= qrow_hi ? qrow_hi / kTile - q_lo + 1 : 0;  // per query head
-    const bool full_range = (q_lo == 0 && n_qh == n_q_total);
-    // The G query heads sharing this key/value head (G = 1 without grouping) are
-    // visited one after the other; dK and dV accumulate over all of them.
-    const int G = prm.H / prm.Hk;
-    const int q_bh0 = (kv_bh / prm.Hk) * prm.H + (kv_bh % prm.Hk) * G;
-    const int b_idx = kv_bh / prm.Hk, hk_idx = kv_bh % prm.Hk;  // batch, key/value head
-    const int bH0 = b_idx * prm.H;  // query head of (batch, head) index bh is bh - bH0
-    const int n_steps = G * n_qh;
-    // Query tile of step t.  Over the full range each key tile starts at its
-    // own index and wraps, so CTAs that run together reduce into different dQ
-    // tiles; otherwise (causal, windows) the range is walked upwards, which
-    // already starts neighbouring key tiles on different query tiles.
-    auto q_tile = [&](int tt) {  // tt: step index within one query head
-        if (!full_range) return q_lo + tt;
-        const int i = j + tt;
-        return i < n_q_total ? i : i - n_q_total;
-    };
+    const BwdWork w(prm);
+    const int j = w.j, n_qh = w.n_qh, q_bh0 = w.q_bh0, b_idx = w.b_idx, hk_idx = w.hk_idx,
+              bH0 = w.bH0, n_steps = w.n_steps;
+    auto q_tile = [&](int tt) { return w.q_tile(tt); };
 
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
@@ -670,6 +693,453 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// 2b. main kernel for d = 128: whole 128-query tiles, pipelined across steps
+// ---------------------------------------------------------------------------
+// Every product is full width (N = 128 queries or features).  An M = 128,
+// N = 128 product with both operands in shared memory reads 8 KB per 64-cycle
+// instruction and runs at the tensor rate, where the 64-query products of the
+// half-tile kernel above read 6 KB per 32 cycles of work and are held to 48
+// cycles by shared-memory bandwidth; the shared-memory traffic of a step drops
+// from about 450 KB to 350 KB.  Per step t (query tile i_t):
+//   S^T(t)  = K Q_t^T          -> region S  (lane = key, column = query)
+//   dP^T(t) = V dO_t^T         -> region dP
+//   dV     += P^T(t) dO_t      (A = P^T, packed bf16 over S^T in region S)
+//   dK     += dS^T(t) Q_t      (A = dS^T, packed bf16 over S^T in region S)
+//   dQ^T(t) = K^T dS^T(t)      -> region dP (lane = feature, column = query)
+// Compute warpgroup h owns query columns 64h .. 64h + 63 of regions S and dP:
+// it packs P^T over the first 32 of its S columns and dS^T over the other 32,
+// so both A operands sit in region S and region dP is free as soon as dP^T has
+// been read.  Issue order of step t:
+//   dV(t), dK(t), dQ^T(t), S^T(t+1), [dQ^T(t) drained], dP^T(t+1),
+//   [P^T(t+1), dS^T(t+1) formed], dV(t+1) ...
+// The dQ writer takes dQ^T(t) out of tensor memory while S^T(t+1) executes, so
+// the drain costs the tensor pipe nothing; the exponentials of step t+1 run
+// while dP^T(t+1) executes, and only the dS^T pass is exposed.  The tensor
+// pipe executes in issue order, so a product that overwrites a region is
+// issued after the last product that reads it.
+// Warps 0-3 / 4-7: compute for query columns 0-63 / 64-127 of the tile (one
+// thread per key row); warps 8-11: dQ writer; warp 12: TMA; warp 13: MMA.
+struct BwdFullTraits {
+    static constexpr int D = 128;
+    static constexpr int BLK_BYTES = kTile * 128;        // one [128 rows x 128 B] block
+    static constexpr int HALF_BYTES = 64 * 128;          // 64 rows of a block
+    static constexpr int TILE_BYTES = kTile * D * 2;
+    static constexpr int DS_BYTES = kTile * kTile * 2;   // dS^T [128 keys][128 queries], 2 blocks
+    static constexpr int STAGES = 2;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + TILE_BYTES;
+    static constexpr int OFF_Q = OFF_V + TILE_BYTES;            // + stage * TILE_BYTES
+    static constexpr int OFF_DO = OFF_Q + STAGES * TILE_BYTES;  // + stage * TILE_BYTES
+    static constexpr int OFF_DS = OFF_DO + STAGES * TILE_BYTES;
+    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;           // -LSE2[s], D[s]: 512 B each
+    static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * 512;
+    // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_full, dq_full,
+    //           dq_empty, dkv_full, done
+    static constexpr int NBARS = 1 + 2 * STAGES + 7;
+    static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
+    static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
+    static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, kTile, false, false);
+    static constexpr uint32_t IDESC_DVK = make_idesc(kFmtBF16, kTile, D, false, true);
+    static constexpr uint32_t IDESC_DQ = make_idesc(kFmtBF16, D, kTile, true, true);
+    static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+};
+
+enum : uint32_t { SITE_DP_FULL = 0x20B };
+
+// Pause of the dQ writer between groups of eight reductions (see the writer).
+constexpr unsigned kDqPauseNs = 60;
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    bwd_main_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                         const BwdParams prm) {
+    using T = BwdFullTraits;
+    constexpr int D = T::D;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + T::OFF_BAR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + T::NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t bar0 = smem_u32(bars);
+    const uint32_t b_kv = bar0;
+    auto b_qdo_full = [&](int s) { return bar0 + 8u * (1 + s); };
+    auto b_qdo_empty = [&](int s) { return bar0 + 8u * (1 + T::STAGES + s); };
+    const uint32_t b_s_full = bar0 + 8u * (1 + 2 * T::STAGES);  // S^T(t) in region S
+    const uint32_t b_dp_full = b_s_full + 8u;                    // dP^T(t) in region dP
+    const uint32_t b_p_full = b_dp_full + 8u;                    // P^T(t), dS^T(t) formed
+    const uint32_t b_dq_full = b_p_full + 8u;                    // dQ^T(t) in region dP
+    const uint32_t b_dq_empty = b_dq_full + 8u;                  // dQ^T(t) read out
+    const uint32_t b_dkv_full = b_dq_empty + 8u;
+    const uint32_t b_done = b_dkv_full + 8u;
+
+    if ((sbase & 1023u) != 0) {
+        if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FE);
+        return;
+    }
+
+    const int N = prm.N;
+    const BwdWork w(prm);
+    const int j = w.j, n_qh = w.n_qh, q_bh0 = w.q_bh0, b_idx = w.b_idx, hk_idx = w.hk_idx,
+              bH0 = w.bH0, n_steps = w.n_steps;
+
+    if (threadIdx.x == 0) {
+        mbar_init(b_kv, 1);
+        for (int s = 0; s < T::STAGES; ++s) {
+            mbar_init(b_qdo_full(s), 1);
+            mbar_init(b_qdo_empty(s), 1);
+        }
+        mbar_init(b_s_full, 1);
+        mbar_init(b_dp_full, 1);
+        mbar_init(b_p_full, 8);    // one arrival per compute warp
+        mbar_init(b_dq_full, 1);
+        mbar_init(b_dq_empty, 4);  // one arrival per dQ-writer warp
+        mbar_init(b_dkv_full, 1);
+        mbar_init(b_done, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 13) {
+        tmem_alloc(smem_u32(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    if (warp == 12 && lane == 0) {
+        tma_prefetch_map(&tm_q);
+        tma_prefetch_map(&tm_k);
+        tma_prefetch_map(&tm_v);
+        tma_prefetch_map(&tm_do);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 12) {
+        // ================= TMA producer =================
+        if (lane == 0) {
+            mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
+            for (int blk = 0; blk < 2; ++blk) {
+                tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
+                            hk_idx, b_idx);
+                tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
+                            hk_idx, b_idx);
+            }
+            int t = 0;
+            int tt = 0, bh = q_bh0;
+            for (; t < n_steps; ++t, ++tt) {
+                if (tt == n_qh) {
+                    tt = 0;
+                    ++bh;
+                }
+                const int s = t % T::STAGES;
+                const int i = w.q_tile(tt);
+                if (t >= T::STAGES &&
+                    !wait_one(b_qdo_empty(s), ((t / T::STAGES) - 1) & 1, abort_flag, prm.st,
+                              SITE_QDO_EMPTY))
+                    break;
+                const uint32_t bf = b_qdo_full(s);
+                mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
+                for (int blk = 0; blk < 2; ++blk) {
+                    tma_load_4d(sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_q, bf,
+                                blk * 64, i * kTile, bh - bH0, b_idx);
+                    tma_load_4d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
+                                blk * 64, i * kTile, bh - bH0, b_idx);
+                }
+                const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile;
+                bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
+                bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
+            }
+            wait_drain(b_kv, 0, prm.st, SITE_DRAIN);
+            const int first = t > T::STAGES ? t - T::STAGES : 0;
+            for (int u = first; u < t; ++u)
+                wait_drain(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, prm.st, SITE_DRAIN);
+        }
+    } else if (warp == 13) {
+        // ================= MMA issuer =================
+        __syncwarp();
+        {
+            const uint32_t tS = tmem + T::COL_S, tDP = tmem + T::COL_DP;
+            const uint32_t tDV = tmem + T::COL_DV, tDK = tmem + T::COL_DK;
+            const uint32_t sK = sbase + T::OFF_K, sV = sbase + T::OFF_V, sDS = sbase + T::OFF_DS;
+            // K-major operand, 16 bf16 (32 bytes) of K per instruction.
+            auto kmaj = [](uint32_t base, int kk) {
+                return desc_add(sw128_desc_words(base, 16, 1024), (kk >> 2) * T::BLK_BYTES + (kk & 3) * 32);
+            };
+            // MN-major operand: rows are the reduction index, 16 rows per instruction.
+            auto mnmaj = [](uint32_t base, int kk) {
+                return desc_add(sw128_desc_words(base, T::BLK_BYTES, 1024), kk * 16 * 128);
+            };
+            auto stage_q = [&](int t) { return sbase + T::OFF_Q + (t % T::STAGES) * T::TILE_BYTES; };
+            auto stage_do = [&](int t) { return sbase + T::OFF_DO + (t % T::STAGES) * T::TILE_BYTES; };
+            // S^T or dP^T: M = 128 keys, N = 128 queries, K = d, both operands K-major.
+            auto issue_sdp = [&](uint32_t d_tmem, uint32_t a, uint32_t b) {
+#pragma unroll
+                for (int q = 0; q < D / 64; ++q)
+                    mma_ss_warp4<false, 0, 2, 4, 6, 0, 2, 4, 6>(d_tmem, kmaj(a, 4 * q), kmaj(b, 4 * q),
+                                                                T::IDESC_SDP, q > 0 ? 1u : 0u);
+            };
+            // dV or dK += A B: A = packed bf16 in tensor memory (queries 0-63 at +0,
+            // 64-127 at +64: each compute warpgroup packs over its own columns), B
+            // MN-major (rows = queries), 16 queries per instruction.
+            auto issue_acc = [&](uint32_t d_tmem, uint32_t a_tmem, uint32_t b, uint32_t accumulate) {
+                mma_ts_warp4<false, 0, 8, 16, 24, 0, 128, 256, 384>(d_tmem, a_tmem, mnmaj(b, 0),
+                                                                    T::IDESC_DVK, accumulate);
+                mma_ts_warp4<false, 0, 8, 16, 24, 0, 128, 256, 384>(d_tmem, a_tmem + 64,
+                                                                    mnmaj(b + T::HALF_BYTES, 0),
+                                                                    T::IDESC_DVK, 1u);
+            };
+            // dQ^T = K^T dS^T: M = d, N = 128 queries, K = 128 keys, both MN-major.
+            auto issue_dq = [&]() {
+#pragma unroll
+                for (int q = 0; q < kTile / 64; ++q)
+                    mma_ss_warp4<false, 0, 128, 256, 384, 0, 128, 256, 384>(
+                        tDP, mnmaj(sK, 4 * q), mnmaj(sDS, 4 * q), T::IDESC_DQ, q > 0 ? 1u : 0u);
+            };
+            auto run = [&]() -> bool {
+                if (n_steps == 0) return true;
+                if (!wait_warp(b_kv, 0, abort_flag, prm.st, SITE_KV) ||
+                    !wait_warp(b_qdo_full(0), 0, abort_flag, prm.st, SITE_QDO_FULL))
+                    return false;
+                tc_fence_after();
+                issue_sdp(tS, sK, stage_q(0));
+                mma_commit_warp(b_s_full);
+                issue_sdp(tDP, sV, stage_do(0));
+                mma_commit_warp(b_dp_full);
+                for (int t = 0; t < n_steps; ++t) {
+                    const uint32_t acc = t > 0 ? 1u : 0u;
+                    if (!wait_warp(b_p_full, t & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                    tc_fence_after();
+                    issue_acc(tDV, tS, stage_do(t), acc);       // dV += P^T(t) dO_t
+                    issue_acc(tDK, tS + 32, stage_q(t), acc);   // dK += dS^T(t) Q_t
+                    mma_commit_warp(b_qdo_empty(t % T::STAGES));
+                    issue_dq();                                 // dQ^T(t), region dP
+                    mma_commit_warp(b_dq_full);
+                    if (t + 1 < n_steps) {
+                        const int u = t + 1;
+                        if (!wait_warp(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, abort_flag, prm.st,
+                                       SITE_QDO_FULL))
+                            return false;
+                        tc_fence_after();
+                        issue_sdp(tS, sK, stage_q(u));          // S^T(t+1) over P^T(t), dS^T(t)
+                        mma_commit_warp(b_s_full);
+                        if (!wait_warp(b_dq_empty, t & 1, abort_flag, prm.st, SITE_DQ_EMPTY)) return false;
+                        tc_fence_after();
+                        issue_sdp(tDP, sV, stage_do(u));        // dP^T(t+1) over dQ^T(t)
+                        mma_commit_warp(b_dp_full);
+                    }
+                }
+                return true;
+            };
+            run();
+            mma_commit_warp(b_dkv_full);
+            mma_commit_warp(b_done);
+            wait_drain(b_done, 0, prm.st, SITE_DRAIN);
+        }
+    } else if (warp < 8) {
+        // ================= compute: P^T, dS^T for query columns 64h .. 64h + 63 =================
+        const int h = warp >> 2;
+        const int wq = warp & 3;
+        const int r = wq * 32 + lane;  // key row within the tile
+        const int kv_row = j * kTile + r;
+        const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
+        const uint32_t tSh = tmem + T::COL_S + 64 * h + lane_off;
+        const uint32_t tDPh = tmem + T::COL_DP + 64 * h + lane_off;
+        const float cs = prm.cs;
+        uint8_t* ds_row = smem + T::OFF_DS + h * T::BLK_BYTES + r * 128;
+        const int sw = r & 7;
+        bool ok = true;
+        for (int t = 0, tt = 0; t < n_steps; ++t, ++tt) {
+            if (tt == n_qh) tt = 0;
+            const int s = t % T::STAGES;
+            const int i = w.q_tile(tt);
+            const float* nlse2 = reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024) + h * 64;
+            const float* dsum = nlse2 + 128;
+            // -LSE2_i and D_i arrived with Q_i/dO_i; waiting on that (completed) phase
+            // makes the bulk-copied bytes visible to this thread.
+            if (!wait_warp(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL) ||
+                !wait_warp(b_s_full, t & 1, abort_flag, prm.st, SITE_S_FULL)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            // query column c of this warpgroup (row qc0 + c) sees key kv_row iff
+            // cmin <= c <= cmax; masked only where some row of the warp needs it
+            const int qc0 = i * kTile + h * 64;
+            const int cmin = prm.win_right < 0 ? -kTile : kv_row - prm.win_right - qc0;
+            const int cmax = prm.win_left < 0 ? 2 * kTile : kv_row + prm.win_left - qc0;
+            const bool masked = __any_sync(0xffffffffu, cmin > 0 || cmax < 63);
+            float p[64];  // P^T of this thread's key row and the warpgroup's 64 queries
+            // Phase A: P^T = 2^(S^T cs - LSE log2 e); packed bf16 over the S^T columns
+            // already read (the A operand of dV), fp32 kept for dS^T.
+            auto phase_a = [&](auto masked_tag, auto cc_tag) {
+                constexpr bool kMasked = decltype(masked_tag)::value;
+                constexpr int cc = decltype(cc_tag)::value;
+                constexpr int c0 = cc * 32;
+                uint32_t sv[32];
+                tmem_ld32(tSh + c0, sv);
+                tmem_ld_wait(sv);
+                uint32_t pk[16];
+                const float4* nl4 = reinterpret_cast<const float4*>(nlse2 + c0);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 nl = nl4[e / 4];  // same address in every lane: broadcast
+                    const float nlv[4] = {nl.x, nl.y, nl.z, nl.w};
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; h2 += 2) {
+                        const int c = c0 + e + h2;
+                        float x0, x1;
+                        ffma2(x0, x1, u2f(sv[e + h2]), u2f(sv[e + h2 + 1]), cs, cs, nlv[h2], nlv[h2 + 1]);
+                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                        if constexpr (kMasked) {
+                            if (c < cmin || c > cmax) p0 = 0.f;
+                            if (c + 1 < cmin || c + 1 > cmax) p1 = 0.f;
+                        }
+                        p[c] = p0;
+                        p[c + 1] = p1;
+                        pk[(e + h2) / 2] = pack_bf16x2(p0, p1);
+                    }
+                }
+                tmem_st16(tSh + 16 * cc, pk);
+            };
+            // Phase B: dS^T = P^T (dP^T - D); packed bf16 over the second 32 of this
+            // warpgroup's S^T columns (read in phase A; the A operand of dK) and into
+            // shared memory with 128-byte swizzle (the B operand of dQ^T, MN-major).
+            auto phase_b = [&](auto cc_tag) {
+                constexpr int cc = decltype(cc_tag)::value;
+                constexpr int c0 = cc * 32;
+                uint32_t dp[32];
+                tmem_ld32(tDPh + c0, dp);
+                tmem_ld_wait(dp);
+                uint32_t dsw[16];
+                const float4* ds4 = reinterpret_cast<const float4*>(dsum + c0);
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    const float4 dd = ds4[e / 4];
+                    const float ddv[4] = {dd.x, dd.y, dd.z, dd.w};
+#pragma unroll
+                    for (int h2 = 0; h2 < 4; h2 += 2) {
+                        const int c = c0 + e + h2;
+                        float t0, t1, d0, d1;
+                        fsub2(t0, t1, u2f(dp[e + h2]), u2f(dp[e + h2 + 1]), ddv[h2], ddv[h2 + 1]);
+                        fmul2(d0, d1, p[c], p[c + 1], t0, t1);
+                        dsw[(e + h2) / 2] = pack_bf16x2(d0, d1);
+                    }
+                }
+                tmem_st16(tSh + 32 + 16 * cc, dsw);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    *reinterpret_cast<uint4*>(ds_row + (((cc * 4 + v) ^ sw) << 4)) =
+                        make_uint4(dsw[4 * v], dsw[4 * v + 1], dsw[4 * v + 2], dsw[4 * v + 3]);
+            };
+            using C0 = std::integral_constant<int, 0>;
+            using C1 = std::integral_constant<int, 1>;
+            if (masked) {
+                phase_a(std::true_type{}, C0{});
+                phase_a(std::true_type{}, C1{});
+            } else {
+                phase_a(std::false_type{}, C0{});
+                phase_a(std::false_type{}, C1{});
+            }
+            if (!wait_warp(b_dp_full, t & 1, abort_flag, prm.st, SITE_DP_FULL)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            phase_b(C0{});
+            phase_b(C1{});
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p_full);
+        }
+        // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled) ----
+        if (ok && wait_warp(b_dkv_full, 0, abort_flag, prm.st, SITE_DKV)) {
+            tc_fence_after();
+            const bool row_ok = kv_row < N;
+            const Strides& ds = h ? prm.dks : prm.dvs;
+            const long long roff = (b_idx * ds.b + hk_idx * ds.h + (row_ok ? kv_row : 0) * ds.n) * 2;
+            const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
+            uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
+            const float f = h ? prm.scale : 1.f;
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(tsrc + 32 * c, o);
+                tmem_ld_wait(o);
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                    pk[e] = n_steps > 0 ? pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f) : 0u;
+                if (row_ok) {
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        st_global_v4(dst + c * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
+                                     pk[4 * v + 3]);
+                }
+            }
+        }
+    } else {
+        // ================= dQ writer (warps 8-11) =================
+        // dQ^T(t) sits in region dP with lane = feature, column = query: warp q
+        // holds features 32q .. 32q + 31 of all 128 queries, so one warp-wide fp32
+        // reduction covers a 128-byte line of the accumulator.  The whole tile
+        // leaves tensor memory before the reductions start, so that dP^T(t+1) can
+        // be issued as soon as possible.
+        const int wq = warp & 3;
+        const uint32_t tq = tmem + T::COL_DP + (static_cast<uint32_t>(wq * 32) << 16);
+        float* acc_col = prm.dq_acc + static_cast<size_t>(wq * 32 + lane);
+        int tt = 0, bh = q_bh0;
+        for (int t = 0; t < n_steps; ++t, ++tt) {
+            if (tt == n_qh) {
+                tt = 0;
+                ++bh;
+            }
+            const int i = w.q_tile(tt);
+            if (!wait_warp(b_dq_full, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) break;
+            tc_fence_after();
+            uint32_t v0[32], v1[32], v2[32], v3[32];
+            tmem_ld32(tq, v0);
+            tmem_ld32(tq + 32, v1);
+            tmem_ld32(tq + 64, v2);
+            tmem_ld32(tq + 96, v3);
+            tmem_ld_wait(v0);
+            tmem_ld_wait(v1);
+            tmem_ld_wait(v2);
+            tmem_ld_wait(v3);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_dq_empty);
+            float* row0 = acc_col + (static_cast<size_t>(bh) * prm.Npad + i * kTile) * D;
+            // The reductions go out in groups of eight with a short pause between
+            // groups: a burst of 128 per thread right after the drain fills the
+            // memory pipeline that the compute warps' shared-memory loads also use
+            // (whole step 2.55 -> 2.27-2.30 ms at B1 H32 N8192 d128).
+            auto send32 = [&](float* rows, const uint32_t (&v)[32]) {
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    red_add_f32(rows + q * D, __uint_as_float(v[q]));
+                    if ((q & 7) == 7) __nanosleep(kDqPauseNs);
+                }
+            };
+            send32(row0, v0);
+            send32(row0 + 32 * D, v1);
+            send32(row0 + 64 * D, v2);
+            send32(row0 + 96 * D, v3);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 13) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
 template <int D>
 cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
@@ -710,13 +1180,22 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
                             cudaStream_t stream) {
     if (D == 64) return launch_bwd_main_impl<64>(tq, tk, tv, tdo, tdq, p, stream);
-    if (D == 128) return launch_bwd_main_impl<128>(tq, tk, tv, tdo, tdq, p, stream);
+    if (D == 128) {
+        using T = BwdFullTraits;
+        static const cudaError_t attr = cudaFuncSetAttribute(
+            bwd_main_full_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+        if (attr != cudaSuccess) return attr;
+        const long long grid = static_cast<long long>(p.BHk) * p.n_kv;
+        bwd_main_full_kernel<<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
+            tq, tk, tv, tdo, p);
+        return cudaGetLastError();
+    }
     return cudaErrorInvalidValue;
 }
 
 int bwd_smem_bytes(int D) {
     if (D == 64) return BwdTraits<64>::SMEM_BYTES;
-    if (D == 128) return BwdTraits<128>::SMEM_BYTES;
+    if (D == 128) return BwdFullTraits::SMEM_BYTES;
     return 0;
 }
 
