@@ -651,6 +651,8 @@ EXTRA_WORKLOADS = {
     "c1_fwd_b1_h1_n128_d64": dict(B=1, H=1, Hk=1, N=128, d=64, causal=False, fwd_only=True),
     "c2_fwd_b4_h16_n1024_d64": dict(B=4, H=16, Hk=16, N=1024, d=64, causal=False, fwd_only=True),
     "c3_causal_b2_h16_n4096_d128": dict(B=2, H=16, Hk=16, N=4096, d=128, causal=True),
+    # the FP8 forward of the step with one group of exponentials in eight on the FMA pipe
+    "fp8_exp2_offload_b1_h16_n16384_d128_causal": dict(fp8=True),
 }
 
 
@@ -797,10 +799,53 @@ def measure_workload(name, steps=20, flush_bytes=512 << 20):
     return comp, f, kind
 
 
+def run_fp8_exp2_offload(args):
+    """FP8 forward of the benchmark step with and without the exponential
+    offload (attn_set_exp2_offload): median device time per call, L2 flushed
+    before each call."""
+    import torch
+
+    from exact_attention_52_gb300 import api
+    from exact_attention_52_gb300.inputs import make_inputs_fp8
+    torch.cuda.set_device(0)
+    f8 = make_inputs_fp8(FP8["B"], FP8["H"], FP8["N"], FP8["d"], seed=0)
+    q8, k8, v8 = (torch.from_numpy(getattr(f8, n)).cuda() for n in ("q8", "k8", "v8"))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    f = attn_flops(FP8["B"], FP8["H"], FP8["N"], FP8["d"], FP8["causal"])
+    comp = {}
+    for on in (False, True):
+        api.set_exp2_offload(on)
+        for _ in range(3):
+            api.fwd_fp8(q8, k8, v8, f8.sq, f8.sk, f8.sv, causal=FP8["causal"])
+        ts = []
+        for _ in range(min(args.steps, 50)):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            api.fwd_fp8(q8, k8, v8, f8.sq, f8.sk, f8.sv, causal=FP8["causal"])
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        ms = statistics.median(ts)
+        comp["exp2_offload" if on else "mufu_only"] = {"ms": round(ms, 5),
+                                                       "tflops": round(f / (ms * 1e-3) / 1e12, 1)}
+    api.set_exp2_offload(False)
+    rc, site = api.check_device_error()
+    if rc != 0:
+        raise RuntimeError(f"device error {rc} at wait site {site:#x}")
+    print(json.dumps({"metric": METRIC, "workload": args.workload, "config": FP8, "unit": "TFLOP/s",
+                      "value": comp["exp2_offload"]["tflops"], "components": comp,
+                      "timing": "median device time per call, L2 flushed before each call",
+                      "dtype": "e4m3", "data": "synthetic"}), flush=True)
+    return 0
+
+
 def run_extra(args):
     """Forward (+ backward) on one of EXTRA_WORKLOADS: a secondary line; the
     default run measures the benchmark step."""
     import torch
+    if args.workload == "fp8_exp2_offload_b1_h16_n16384_d128_causal":
+        return run_fp8_exp2_offload(args)
     torch.cuda.set_device(0)
     comp, f, kind = measure_workload(args.workload, steps=min(args.steps, 50))
     main_ms = comp.get("fwd", comp.get("fwd_splitkv"))["ms"] + comp.get("bwd", {}).get("ms", 0.0)

@@ -15,6 +15,8 @@ import os
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libattn_sm103a.so")
+# The same library built with device-side range checks (see attn_build_flags).
+DEBUG_LIB_PATH = os.path.join(_PKG, "libattn_sm103a_debug.so")
 
 ATTN_OK = 0
 STATUS_NAMES = {0: "ATTN_OK", -1: "ATTN_ERR_INVALID", -2: "ATTN_ERR_UNSUPPORTED",
@@ -54,9 +56,11 @@ SIGNATURES = {
     "attn_fwd_fp8": (_i, [_vp, _vp, _vp, _f, _f, _f, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp]),
     "attn_check_device_error": (_i, [_vp, ctypes.POINTER(ctypes.c_uint)]),
     "attn_set_wait_limit_ns": (None, [ctypes.c_ulonglong]),
+    "attn_set_exp2_offload": (None, [_i]),
     "attn_selftest_wait_timeout": (_i, [_vp]),
     "attn_status_string": (ctypes.c_char_p, [_i]),
     "attn_kernel_smem_bytes": (_i, [_i, _i]),
+    "attn_build_flags": (_i, []),
 }
 
 _lib = None
@@ -279,6 +283,11 @@ def check_device_error(stream=None) -> tuple[int, int]:
 
 def set_wait_limit_ns(ns: int) -> None:
     load_library().attn_set_wait_limit_ns(int(ns))
+
+
+def set_exp2_offload(on: bool) -> None:
+    """FP8 forward: compute one group of exponentials in eight on the FMA pipe."""
+    load_library().attn_set_exp2_offload(int(bool(on)))
 
 
 def selftest_wait_timeout(stream=None) -> None:

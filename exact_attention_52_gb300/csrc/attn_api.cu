@@ -20,6 +20,7 @@ __device__ unsigned int g_err_word[2];
 
 constexpr unsigned long long kDefaultWaitLimitNs = 1000000000ull;
 unsigned long long g_wait_limit_ns = kDefaultWaitLimitNs;
+int g_exp2_offload = 0;  // attn_set_exp2_offload
 
 constexpr int kMaxDevices = 64;
 
@@ -254,6 +255,7 @@ attn_status fwd_run(const void* q, const Strides& qs, const void* k, const Strid
     p.split_len = split.n_splits > 1 ? split.split_len : (N + kTile - 1) / kTile;
     p.o_part = split.o_part;
     p.lse_part = split.lse_part;
+    p.exp2_offload = 0;
     p.st = dev_status(ds);
     return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
@@ -574,6 +576,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
     p.split_len = (N + kTile - 1) / kTile;
     p.o_part = nullptr;
     p.lse_part = nullptr;
+    p.exp2_offload = g_exp2_offload;
     p.st = dev_status(ds);
     return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
@@ -668,6 +671,8 @@ attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site) {
     return host[0] ? ATTN_ERR_TIMEOUT : ATTN_OK;
 }
 
+void attn_set_exp2_offload(int on) { g_exp2_offload = on ? 1 : 0; }
+
 void attn_set_wait_limit_ns(unsigned long long ns) {
     g_wait_limit_ns = ns ? ns : kDefaultWaitLimitNs;
 }
@@ -691,6 +696,8 @@ const char* attn_status_string(attn_status s) {
     }
     return "ATTN_ERR_UNKNOWN";
 }
+
+int attn_build_flags(void) { return kDebugChecks ? 1 : 0; }
 
 int attn_kernel_smem_bytes(int which, int d) {
     if (which == 0) return fwd_smem_bytes(d, false);

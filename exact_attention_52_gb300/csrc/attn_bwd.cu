@@ -313,10 +313,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
             for (int blk = 0; blk < T::NBLK; ++blk) {
-                tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
-                            hk_idx, b_idx);
-                tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
-                            hk_idx, b_idx);
+                const int B = prm.BHk / prm.Hk;
+                if (dbg_tma(sbase + T::OFF_K + blk * T::BLK_BYTES, blk * 64, j * kTile, hk_idx, b_idx, D, N,
+                            prm.Hk, B, 2, 0x2D1))
+                    tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
+                                hk_idx, b_idx);
+                if (dbg_tma(sbase + T::OFF_V + blk * T::BLK_BYTES, blk * 64, j * kTile, hk_idx, b_idx, D, N,
+                            prm.Hk, B, 2, 0x2D2))
+                    tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
+                                hk_idx, b_idx);
             }
             int t = 0;
             int tt = 0, bh = q_bh0;  // step t = (head bh - q_bh0) * n_qh + tt
@@ -333,15 +338,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 const uint32_t bf = b_qdo_full(s);
                 mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
+                const int B = prm.BHk / prm.Hk;
                 for (int blk = 0; blk < T::NBLK; ++blk) {
-                    tma_load_4d(sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_q, bf,
-                                blk * 64, i * kTile, bh - bH0, b_idx);
-                    tma_load_4d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
-                                blk * 64, i * kTile, bh - bH0, b_idx);
+                    const uint32_t dq_ = sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES;
+                    const uint32_t ddo = sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES;
+                    if (dbg_tma(dq_, blk * 64, i * kTile, bh - bH0, b_idx, D, N, prm.H, B, 2, 0x2D3))
+                        tma_load_4d(dq_, &tm_q, bf, blk * 64, i * kTile, bh - bH0, b_idx);
+                    if (dbg_tma(ddo, blk * 64, i * kTile, bh - bH0, b_idx, D, N, prm.H, B, 2, 0x2D4))
+                        tma_load_4d(ddo, &tm_do, bf, blk * 64, i * kTile, bh - bH0, b_idx);
                 }
                 const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile;
-                bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
-                bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
+                if (dbg_ok(vrow + kTile <= static_cast<size_t>(B) * prm.H * prm.Npad, 0x2D5)) {
+                    bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
+                    bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
+                }
             }
             wait_drain(b_kv, 0, prm.st, SITE_DRAIN);
             const int first = t > T::STAGES ? t - T::STAGES : 0;
@@ -670,7 +680,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                                                  (u < SLOTS_PER_BUF ? T::OFF_Q + s * T::TILE_BYTES + u * 16384
                                                                     : T::OFF_DO + s * T::TILE_BYTES +
                                                                           (u - SLOTS_PER_BUF) * 16384);
-                            tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
+                            if (dbg_ok(p * 64 + 32 * b < D && i * kTile < prm.Npad &&
+                                           bh < (prm.BHk / prm.Hk) * prm.H,
+                                       0x2D6))
+                                tma_reduce_add_3d(&tm_dq, box, p * 64 + 32 * b, i * kTile, bh);
                         }
                         bulk_commit_group();
                     }
@@ -822,10 +835,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (lane == 0) {
             mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
             for (int blk = 0; blk < 2; ++blk) {
-                tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
-                            hk_idx, b_idx);
-                tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
-                            hk_idx, b_idx);
+                const int B = prm.BHk / prm.Hk;
+                if (dbg_tma(sbase + T::OFF_K + blk * T::BLK_BYTES, blk * 64, j * kTile, hk_idx, b_idx, D, N,
+                            prm.Hk, B, 2, 0x2D1))
+                    tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
+                                hk_idx, b_idx);
+                if (dbg_tma(sbase + T::OFF_V + blk * T::BLK_BYTES, blk * 64, j * kTile, hk_idx, b_idx, D, N,
+                            prm.Hk, B, 2, 0x2D2))
+                    tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
+                                hk_idx, b_idx);
             }
             int t = 0;
             int tt = 0, bh = q_bh0;
@@ -842,15 +860,20 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     break;
                 const uint32_t bf = b_qdo_full(s);
                 mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
+                const int B = prm.BHk / prm.Hk;
                 for (int blk = 0; blk < 2; ++blk) {
-                    tma_load_4d(sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_q, bf,
-                                blk * 64, i * kTile, bh - bH0, b_idx);
-                    tma_load_4d(sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES, &tm_do, bf,
-                                blk * 64, i * kTile, bh - bH0, b_idx);
+                    const uint32_t dq_ = sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES;
+                    const uint32_t ddo = sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES;
+                    if (dbg_tma(dq_, blk * 64, i * kTile, bh - bH0, b_idx, D, N, prm.H, B, 2, 0x2D3))
+                        tma_load_4d(dq_, &tm_q, bf, blk * 64, i * kTile, bh - bH0, b_idx);
+                    if (dbg_tma(ddo, blk * 64, i * kTile, bh - bH0, b_idx, D, N, prm.H, B, 2, 0x2D4))
+                        tma_load_4d(ddo, &tm_do, bf, blk * 64, i * kTile, bh - bH0, b_idx);
                 }
                 const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile;
-                bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
-                bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
+                if (dbg_ok(vrow + kTile <= static_cast<size_t>(B) * prm.H * prm.Npad, 0x2D5)) {
+                    bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
+                    bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
+                }
             }
             wait_drain(b_kv, 0, prm.st, SITE_DRAIN);
             const int first = t > T::STAGES ? t - T::STAGES : 0;
@@ -1149,6 +1172,8 @@ cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, c
         bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     const long long grid = static_cast<long long>(p.BHk) * p.n_kv;
+    const cudaError_t dbg = dbg_set_word(p.st.word, stream);
+    if (dbg != cudaSuccess) return dbg;
     bwd_main_kernel<D><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(tq, tk, tv, tdo, tdq,
                                                                                         p);
     return cudaGetLastError();
@@ -1186,6 +1211,8 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
             bwd_main_full_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
         if (attr != cudaSuccess) return attr;
         const long long grid = static_cast<long long>(p.BHk) * p.n_kv;
+        const cudaError_t dbg = dbg_set_word(p.st.word, stream);
+        if (dbg != cudaSuccess) return dbg;
         bwd_main_full_kernel<<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
             tq, tk, tv, tdo, p);
         return cudaGetLastError();

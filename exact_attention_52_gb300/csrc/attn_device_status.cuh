@@ -13,6 +13,8 @@ namespace attn {
 enum : uint32_t {
     ATTN_DEVERR_WAIT_TIMEOUT = 1u,  // a bounded mbarrier wait gave up
     ATTN_DEVERR_SMEM_ALIGN = 2u,    // dynamic shared memory was not 1024-byte aligned
+    ATTN_DEVERR_RANGE = 4u,         // debug builds: a TMA coordinate or tensor-memory address
+                                    // failed its range check (the access was skipped)
 };
 
 struct DevStatus {

@@ -45,6 +45,10 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kRedoBound = 1152921504606846976.0f;  // 2^60
 constexpr float kRedoBoundFP8 = 448.0f;                 // largest finite E4M3 value
+// With the exponential offload on (FMAEXP), the group of four columns (offset
+// within each 32) whose exponentials run on the FMA pipe (ex2_fma2) instead of
+// MUFU: one group in eight.
+constexpr int kFmaExpGroup = 28;
 
 template <int D, bool FP8>
 struct FwdTraits {
@@ -80,7 +84,7 @@ enum : uint32_t {
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool FMAEXP>
 __global__ void __launch_bounds__(320, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, const FwdParams prm) {
@@ -233,10 +237,13 @@ __global__ void __launch_bounds__(320, 1)
                             return false;
                         mbar_arrive_expect_tx(b_kv_full(slot), T::TILE_BYTES);
                         const CUtensorMap* map = t ? &tm_v : &tm_k;
-                        for (int blk = 0; blk < T::NBLK; ++blk)
-                            tma_load_4d(smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES), map,
-                                        b_kv_full(slot), blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile,
-                                        it.hk_idx, it.b_idx);
+                        for (int blk = 0; blk < T::NBLK; ++blk) {
+                            const uint32_t dst = smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES);
+                            if (dbg_tma(dst, blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile, it.hk_idx, it.b_idx, D,
+                                        N, prm.Hk, prm.BH / prm.H, T::EB, 0x1D1))
+                                tma_load_4d(dst, map, b_kv_full(slot), blk * T::BLK_ELEMS,
+                                            (it.kv_lo + j) * kTile, it.hk_idx, it.b_idx);
+                        }
                     }
                     return true;
                 };
@@ -254,9 +261,13 @@ __global__ void __launch_bounds__(320, 1)
                 mbar_arrive_expect_tx(b_q, q_tiles * T::TILE_BYTES);
                 for (int g = 0; g < 2; ++g) {
                     if (it.n(g) == 0) continue;
-                    for (int blk = 0; blk < T::NBLK; ++blk)
-                        tma_load_4d(smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES), &tm_q, b_q,
-                                    blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile, it.h_idx, it.b_idx);
+                    for (int blk = 0; blk < T::NBLK; ++blk) {
+                        const uint32_t dst = smem_u32(sQ + g * T::TILE_BYTES + blk * T::BLK_BYTES);
+                        if (dbg_tma(dst, blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile, it.h_idx, it.b_idx, D,
+                                    N, prm.H, prm.BH / prm.H, T::EB, 0x1D2))
+                            tma_load_4d(dst, &tm_q, b_q, blk * T::BLK_ELEMS, (2 * it.pair + g) * kTile,
+                                        it.h_idx, it.b_idx);
+                    }
                 }
                 for (int j = 1; j < it.n_kv && ok; ++j) ok = load_kv(j);
                 ++k;
@@ -573,8 +584,17 @@ __global__ void __launch_bounds__(320, 1)
                         float x0, x1, x2, x3;
                         ffma2(x0, x1, u2f(s[c][i]), u2f(s[c][i + 1]), cs, cs, -m_sub, -m_sub);
                         ffma2(x2, x3, u2f(s[c][i + 2]), u2f(s[c][i + 3]), cs, cs, -m_sub, -m_sub);
-                        const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+                        float p0, p1, p2, p3;
+                        if (FMAEXP && i == kFmaExpGroup) {
+                            // one group of four in eight: exponentials on the FMA pipe
+                            ex2_fma2(p0, p1, x0, x1);
+                            ex2_fma2(p2, p3, x2, x3);
+                        } else {
+                            p0 = ex2_approx(x0);
+                            p1 = ex2_approx(x1);
+                            p2 = ex2_approx(x2);
+                            p3 = ex2_approx(x3);
+                        }
                         if constexpr (FP8) {
                             pk0[c * 8 + i / 4] = pack_e4m3x4(p0, p1, p2, p3);
                         } else {
@@ -750,12 +770,12 @@ __global__ void __launch_bounds__(256) splitkv_combine_kernel(const CombineParam
     }
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool FMAEXP = false>
 cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, cudaStream_t stream) {
     using T = FwdTraits<D, FP8>;
     static const cudaError_t attr = cudaFuncSetAttribute(
-        fwd_kernel<D, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+        fwd_kernel<D, FP8, FMAEXP>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
     if (attr != cudaSuccess) return attr;
     // Persistent CTAs, one per SM (shared memory admits one), each looping over
     // items in the snake order of item_at: equal items (no mask) and longest-first
@@ -770,7 +790,9 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
         if (sms < grid) grid = sms;
     }
     if (grid < 1) return cudaSuccess;
-    fwd_kernel<D, FP8><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+    const cudaError_t dbg = dbg_set_word(p.st.word, stream);
+    if (dbg != cudaSuccess) return dbg;
+    fwd_kernel<D, FP8, FMAEXP><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }
 
@@ -785,7 +807,9 @@ cudaError_t launch_fwd_bf16(int D, const CUtensorMap& tq, const CUtensorMap& tk,
 
 cudaError_t launch_fwd_fp8(int D, const CUtensorMap& tq, const CUtensorMap& tk,
                            const CUtensorMap& tv, const FwdParams& p, cudaStream_t stream) {
-    if (D == 128) return launch_fwd_impl<128, true>(tq, tk, tv, p, stream);
+    if (D == 128)
+        return p.exp2_offload ? launch_fwd_impl<128, true, true>(tq, tk, tv, p, stream)
+                              : launch_fwd_impl<128, true>(tq, tk, tv, p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -36,6 +36,7 @@ struct FwdParams {
     int split_len;
     float* o_part;    // fp32 [n_splits, BH, N, D]
     float* lse_part;  // fp32 [n_splits, BH, N]; -inf where a split saw no key
+    int exp2_offload; // FP8: one group of four exponentials in eight on the FMA pipe
     DevStatus st;
 };
 

@@ -8,10 +8,69 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cuda_runtime.h>
 
 #include "attn_device_status.cuh"
 
 namespace attn {
+
+// ---------------------------------------------------------------------------
+// Debug builds (ATTN_DEBUG_CHECKS): range checks on every TMA coordinate and
+// tensor-memory address, standing in for a memory checker.  A failed check
+// ORs ATTN_DEVERR_RANGE into the device error word, records the check's site
+// id and skips the access; nothing traps.  Release builds compile them away.
+// ---------------------------------------------------------------------------
+#ifdef ATTN_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+// The error word of the launching call, copied in by this file's launchers.
+static __device__ unsigned int* g_dbg_word;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ bool dbg_ok(bool cond, uint32_t site) {
+#ifdef ATTN_DEBUG_CHECKS
+    if (!cond) {
+        if (g_dbg_word != nullptr) record_device_error(g_dbg_word, ATTN_DEVERR_RANGE, site);
+        return false;
+    }
+#endif
+    (void)site;
+    return true;
+}
+
+// A 32x32b tensor-memory access of `ncols` columns by this warp: the lanes are
+// the warp's own quadrant and the columns lie inside the 512 every kernel of
+// the library allocates (the allocation then starts at column 0).
+__device__ __forceinline__ bool dbg_tmem(uint32_t taddr, uint32_t ncols, uint32_t site) {
+    if constexpr (!kDebugChecks) return true;
+    const uint32_t lane = taddr >> 16, col = taddr & 0xFFFFu;
+    return dbg_ok(lane == ((threadIdx.x >> 5) & 3u) * 32u && col + ncols <= 512u, site);
+}
+
+// A TMA box load at element coordinates {x, row, head, batch} of a
+// {d, N, heads, B} view: x on a 16-byte boundary and inside the row, the box's
+// first row inside the sequence (later rows may fall past it: they read as
+// zero), head and batch inside the tensor, destination 1024-byte aligned.
+__device__ __forceinline__ bool dbg_tma(uint32_t dst, int x, int row, int head, int batch, int d, int N,
+                                        int heads, int B, int elem_bytes, uint32_t site) {
+    if constexpr (!kDebugChecks) return true;
+    return dbg_ok((dst & 1023u) == 0 && x >= 0 && (x * elem_bytes) % 16 == 0 && x < d && row >= 0 &&
+                      row < N && head >= 0 && head < heads && batch >= 0 && batch < B,
+                  site);
+}
+
+// Debug builds: point the range checks of the calling file at the launching
+// call's error word (a small copy on the launch stream, ahead of the kernel).
+inline cudaError_t dbg_set_word(unsigned int* word, cudaStream_t stream) {
+#ifdef ATTN_DEBUG_CHECKS
+    return cudaMemcpyToSymbolAsync(g_dbg_word, &word, sizeof(word), 0, cudaMemcpyHostToDevice, stream);
+#else
+    (void)word;
+    (void)stream;
+    return cudaSuccess;
+#endif
+}
 
 // ---------------------------------------------------------------------------
 // Addresses
@@ -223,6 +282,7 @@ __device__ __forceinline__ void tc_fence_after() {
 // 32 consecutive 32-bit columns of this warp's 32 lanes (one lane per thread).
 // The values are valid only after tmem_ld_wait() on the same array.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    if (!dbg_tmem(taddr, 32, 0xD01)) return;
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
                  : "r"(taddr));
@@ -237,6 +297,7 @@ __device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    if (!dbg_tmem(taddr, 32, 0xD02)) return;
     asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};"
                  :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
                  : "memory");
@@ -244,6 +305,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 // 16 consecutive 32-bit columns (one lane per thread).
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    if (!dbg_tmem(taddr, 16, 0xD03)) return;
     asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
                  :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
                  : "memory");
@@ -324,6 +386,9 @@ template <bool FP8, uint32_t OA0, uint32_t OA1, uint32_t OA2, uint32_t OA3, uint
           uint32_t OB2, uint32_t OB3>
 __device__ __forceinline__ void mma_ss_warp4(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc,
                                              uint32_t accumulate) {
+    // D: lane 0 (M = 128 rows from lane 0), N fp32 columns inside the allocation
+    if (!dbg_ok((d_tmem >> 16) == 0 && (d_tmem & 0xFFFFu) + ((idesc >> 17) & 0x3Fu) * 8u <= 512u, 0xD04))
+        return;
     if constexpr (FP8) {
         asm volatile(
             "{\n\t.reg .pred p, t, e;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
@@ -363,6 +428,12 @@ template <bool FP8, uint32_t OA0, uint32_t OA1, uint32_t OA2, uint32_t OA3, uint
           uint32_t OB2, uint32_t OB3>
 __device__ __forceinline__ void mma_ts_warp4(uint32_t d_tmem, uint32_t a_tmem, SmemDesc b, uint32_t idesc,
                                              uint32_t accumulate) {
+    // D as above; A: 8 columns (16 bf16 or 32 e4m3 values of K per row) at each of
+    // the four offsets, lanes from 0
+    if (!dbg_ok((d_tmem >> 16) == 0 && (d_tmem & 0xFFFFu) + ((idesc >> 17) & 0x3Fu) * 8u <= 512u &&
+                    (a_tmem >> 16) == 0 && (a_tmem & 0xFFFFu) + OA3 + 8u <= 512u,
+                0xD05))
+        return;
     if constexpr (FP8) {
         asm volatile(
             "{\n\t.reg .pred p, t, e;\n\t.reg .b32 ta, bl;\n\t.reg .b64 db;\n\t"
@@ -474,6 +545,33 @@ __device__ __forceinline__ void fsub2(float& d0, float& d1, float a0, float a1, 
         "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
         : "=f"(d0), "=f"(d1)
         : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// 2^x for two floats on the FMA pipe instead of MUFU (the softmax of the
+// forward pass is bound by MUFU: one ex2 per element at a quarter of the issue
+// rate, so moving a few of them to the otherwise idle FMA pipe shortens it).
+// x = n + r with n = round(x): adding 1.5 * 2^23 leaves n in the low mantissa
+// bits of t (the float spacing there is 1), so t - 1.5 * 2^23 = n exactly and
+// r = x - n lies in [-1/2, 1/2].  2^r comes from a cubic fitted here to the
+// relative error of 2^r on that interval (Lawson's iteratively reweighted least
+// squares; max relative error 7.5e-5, also in fp32 evaluation), and n is added
+// to the exponent field: the low bits of t shifted up by 23 are n << 23 modulo
+// 2^32.  x is clamped below at -125 so that the exponent field stays positive;
+// results under 2^-125 (zero in every use here) come out as about 2^-125.
+__device__ __forceinline__ void ex2_fma2(float& y0, float& y1, float x0, float x1) {
+    constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+    constexpr float c0 = 0.99992812f, c1 = 0.69326097f, c2 = 0.24261054f, c3 = 0.055171322f;
+    x0 = fmaxf(x0, -125.f);
+    x1 = fmaxf(x1, -125.f);
+    float t0, t1, n0, n1, r0, r1, p0, p1;
+    fadd2(t0, t1, x0, x1, kRound, kRound);
+    fsub2(n0, n1, t0, t1, kRound, kRound);
+    fsub2(r0, r1, x0, x1, n0, n1);
+    ffma2(p0, p1, r0, r1, c3, c3, c2, c2);
+    ffma2(p0, p1, p0, p1, r0, r1, c1, c1);
+    ffma2(p0, p1, p0, p1, r0, r1, c0, c0);
+    y0 = __int_as_float(__float_as_int(p0) + (__float_as_int(t0) << 23));
+    y1 = __int_as_float(__float_as_int(p1) + (__float_as_int(t1) << 23));
 }
 
 // acc + lo(w) + hi(w) where w holds two bf16 values: mixed-precision adds

@@ -264,6 +264,19 @@ attn_status attn_check_device_error(attn_stream_t stream, unsigned int* site);
 void attn_set_wait_limit_ns(unsigned long long ns);
 
 /*
+ * Exponential offload of the FP8 forward (later attn_fwd_fp8 calls; default
+ * off): with on != 0, one group of four score columns in eight computes its
+ * exponentials on the FMA pipe (2^x = 2^n 2^r, n = round(x), 2^r from a cubic
+ * with relative error below 7.5e-5) instead of the MUFU unit.  Results stay
+ * within the FP8 tolerance either way.  Off by default because it measured
+ * slower on GB300 (B1 H16 N16384 d128 causal: 0.588 vs 0.533 ms): the softmax
+ * pass is bound by instruction issue and latency, not by MUFU throughput.
+ * Source: kernaut-resources wiki, FlashAttention-3 code walkthrough README,
+ * technique tag "software-exp" (exponentials emulated on the FMA units).
+ */
+void attn_set_exp2_offload(int on);
+
+/*
  * Self-test of the bounded-wait path: launches one CTA whose warps wait on a
  * barrier nothing ever completes, with the current wait limit.  The kernel
  * returns after the limit; attn_check_device_error() must then report
@@ -277,6 +290,17 @@ const char* attn_status_string(attn_status s);
 /* Dynamic shared memory (bytes) one CTA of the given kernel requests:
  * which = 0 forward bf16, 1 forward fp8, 2 backward main; 0 if not built. */
 int attn_kernel_smem_bytes(int which, int d);
+
+/* How this copy of the library was built.  Bit 0: device-side range checks
+ * (libattn_sm103a_debug.so): every TMA box coordinate is checked against the
+ * tensor's extents and 16-byte rule, and every tensor-memory access and MMA
+ * operand address against the warp's lane quadrant and the 512 allocated
+ * columns.  A failed check skips the access and makes the next
+ * attn_check_device_error() return ATTN_ERR_TIMEOUT with the check's site id
+ * (0xD01-0xD05 tensor memory, 0x1D1-0x1D2 and 0x2D1-0x2D6 TMA and bulk copies);
+ * it never traps.  The checks stand in for a memory checker in tests; the
+ * release library has none (bit 0 clear).  The pages describe no such build. */
+int attn_build_flags(void);
 
 #ifdef __cplusplus
 }

@@ -74,3 +74,27 @@ def test_fp8_fwd_growing_scores_exercise_rescale(causal):
     assert np.all(np.isfinite(o))
     assert rel_fro(o, o_ref) <= TOL_FP8_RELFRO, rel_fro(o, o_ref)
     assert max_abs(lse, lse_ref) <= TOL_LSE_ABS, max_abs(lse, lse_ref)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("N", [100, 300, 2000])
+def test_fp8_fwd_exp2_offload_matches_oracle(N, causal):
+    """attn_set_exp2_offload(1): one group of four exponentials in eight is
+    computed on the FMA pipe (2^n times a cubic for 2^r).  The outputs must
+    meet the same FP8 tolerances, and differ from the MUFU path only by the
+    polynomial's relative error (7.5e-5) passed through the E4M3 rounding of P."""
+    inp = make_inputs_fp8(2, 2, N, 128, seed=70 + N + int(causal))
+    o_ref_gpu, lse_ref_gpu = run_fp8(inp, causal)
+    api.set_exp2_offload(True)
+    try:
+        o, lse = run_fp8(inp, causal)
+    finally:
+        api.set_exp2_offload(False)
+    q, k, v = decoded_fp8(inp)
+    o_ref, lse_ref = oracle.forward(q, k, v, 1.0 / np.sqrt(128), causal)
+    assert rel_fro(o, o_ref) <= TOL_FP8_RELFRO, rel_fro(o, o_ref)
+    assert max_abs(lse, lse_ref) <= TOL_LSE_ABS, max_abs(lse, lse_ref)
+    # the two GPU paths: P rounded to E4M3 can flip by one code where the
+    # polynomial lands on the other side of a rounding boundary
+    assert rel_fro(o, o_ref_gpu) <= 1e-2
+    assert max_abs(lse, lse_ref_gpu) <= 1e-4
