@@ -938,6 +938,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     issue_acc(tDV, tS, stage_do(t), acc);       // dV += P^T(t) dO_t
                     issue_acc(tDK, tS + 32, stage_q(t), acc);   // dK += dS^T(t) Q_t
                     mma_commit_warp(b_qdo_empty(t % T::STAGES));
+                    // dV, dK are final after the last step's products: the epilogue may
+                    // start while the last dQ product and its reductions run
+                    if (t + 1 == n_steps) mma_commit_warp(b_dkv_full);
                     issue_dq();                                 // dQ^T(t), region dP
                     mma_commit_warp(b_dq_full);
                     if (t + 1 < n_steps) {
@@ -956,8 +959,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 return true;
             };
-            run();
-            mma_commit_warp(b_dkv_full);
+            // dkv_full is committed after the last dK product (inside run()); when the
+            // loop ended early (a wait gave up) or never ran, commit it here instead
+            if (!run() || n_steps == 0) mma_commit_warp(b_dkv_full);
             mma_commit_warp(b_done);
             wait_drain(b_done, 0, prm.st, SITE_DRAIN);
         }
@@ -1140,12 +1144,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // The reductions go out in groups of eight with a short pause between
             // groups: a burst of 128 per thread right after the drain fills the
             // memory pipeline that the compute warps' shared-memory loads also use
-            // (whole step 2.55 -> 2.27-2.30 ms at B1 H32 N8192 d128).
+            // (whole step 2.55 -> 2.27-2.30 ms at B1 H32 N8192 d128).  The last
+            // step's reductions compete with nothing but the epilogue: no pauses.
+            const bool pace = t + 1 < n_steps;
             auto send32 = [&](float* rows, const uint32_t (&v)[32]) {
 #pragma unroll
                 for (int q = 0; q < 32; ++q) {
                     red_add_f32(rows + q * D, __uint_as_float(v[q]));
-                    if ((q & 7) == 7) __nanosleep(kDqPauseNs);
+                    if ((q & 7) == 7 && pace) __nanosleep(kDqPauseNs);
                 }
             };
             send32(row0, v0);
