@@ -191,14 +191,18 @@ struct BwdWork {
     int bH0;             // (batch, head) index of head 0 of this batch
     int n_steps;         // G * n_qh
 
-    __device__ explicit BwdWork(const BwdParams& prm) {
+    __device__ explicit BwdWork(const BwdParams& prm) : BwdWork(prm, static_cast<int>(blockIdx.x)) {}
+
+    // Work item `item` of the launch's numbering (items = key tiles of every
+    // key/value head).
+    __device__ BwdWork(const BwdParams& prm, int item) {
         const int N = prm.N;
         // Non-causal: head-major order keeps the resident CTAs on a few heads, so
         // those heads' Q, dO and fp32 dQ accumulator stay in L2 while every key
         // tile reduces into them.  Causal: low key tiles (longest loops) of every
         // head first, which keeps the tail of the launch short.
-        kv_bh = prm.causal ? static_cast<int>(blockIdx.x % prm.BHk) : static_cast<int>(blockIdx.x / prm.n_kv);
-        j = prm.causal ? static_cast<int>(blockIdx.x / prm.BHk) : static_cast<int>(blockIdx.x % prm.n_kv);
+        kv_bh = prm.causal ? item % prm.BHk : item / prm.n_kv;
+        j = prm.causal ? item / prm.BHk : item % prm.n_kv;
         n_q_total = (N + kTile - 1) / kTile;
         // Query tiles holding the rows that see some key of this tile (window
         // i - win_left <= key <= i + win_right; negative = no bound).
@@ -748,8 +752,8 @@ struct BwdFullTraits {
     static constexpr int OFF_VEC = OFF_DS + DS_BYTES;           // -LSE2[s], D[s]: 512 B each
     static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * 512;
     // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_full, dq_full,
-    //           dq_empty, dkv_full, done
-    static constexpr int NBARS = 1 + 2 * STAGES + 7;
+    //           dq_empty, dkv_full, done, kv_empty
+    static constexpr int NBARS = 1 + 2 * STAGES + 8;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
     static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, kTile, false, false);
@@ -758,7 +762,7 @@ struct BwdFullTraits {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-enum : uint32_t { SITE_DP_FULL = 0x20B };
+enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C };
 
 // Pause of the dQ writer between groups of eight reductions (see the writer).
 constexpr unsigned kDqPauseNs = 60;
@@ -788,6 +792,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t b_dq_empty = b_dq_full + 8u;                  // dQ^T(t) read out
     const uint32_t b_dkv_full = b_dq_empty + 8u;
     const uint32_t b_done = b_dkv_full + 8u;
+    const uint32_t b_kv_empty = b_done + 8u;                     // an item's K, V read for the last time
 
     if ((sbase & 1023u) != 0) {
         if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FE);
@@ -795,12 +800,25 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 
     const int N = prm.N;
-    const BwdWork w(prm);
-    const int j = w.j, n_qh = w.n_qh, q_bh0 = w.q_bh0, b_idx = w.b_idx, hk_idx = w.hk_idx,
-              bH0 = w.bH0, n_steps = w.n_steps;
+    // Persistent CTAs: CTA c takes the items of the launch's numbering (key tiles
+    // of every key/value head; non-causal head-major, causal longest first) in
+    // rounds of G = gridDim.x, dealt in snake order (CTA c takes item rG + c in
+    // even rounds and rG + G - 1 - c in odd ones), so that longest-first causal
+    // items leave every CTA within about one item of the others.  An item's
+    // epilogue (dV, dK out of tensor memory) overlaps the next item's K/V copy
+    // and first products.  item_at returns -1 after the last round and -2 for a
+    // round in which this CTA has no item (only the last round can be short).
+    const int n_items = prm.BHk * prm.n_kv;
+    auto item_at = [&](int r) -> int {
+        const long long base = static_cast<long long>(r) * gridDim.x;
+        if (base >= n_items) return -1;
+        const int c = (r & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+        return base + c < n_items ? static_cast<int>(base + c) : -2;
+    };
 
     if (threadIdx.x == 0) {
         mbar_init(b_kv, 1);
+        mbar_init(b_kv_empty, 1);
         for (int s = 0; s < T::STAGES; ++s) {
             mbar_init(b_qdo_full(s), 1);
             mbar_init(b_qdo_empty(s), 1);
@@ -830,37 +848,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // Steps are counted over all of the CTA's items (g): the Q/dO stages and the
+    // per-step barriers run on through item boundaries.
     if (warp == 12) {
         // ================= TMA producer =================
         if (lane == 0) {
-            mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
-            for (int blk = 0; blk < 2; ++blk) {
-                const int B = prm.BHk / prm.Hk;
-                if (dbg_tma(sbase + T::OFF_K + blk * T::BLK_BYTES, blk * 64, j * kTile, hk_idx, b_idx, D, N,
-                            prm.Hk, B, 2, 0x2D1))
-                    tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, j * kTile,
-                                hk_idx, b_idx);
-                if (dbg_tma(sbase + T::OFF_V + blk * T::BLK_BYTES, blk * 64, j * kTile, hk_idx, b_idx, D, N,
-                            prm.Hk, B, 2, 0x2D2))
-                    tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, j * kTile,
-                                hk_idx, b_idx);
-            }
-            int t = 0;
-            int tt = 0, bh = q_bh0;
-            for (; t < n_steps; ++t, ++tt) {
-                if (tt == n_qh) {
-                    tt = 0;
-                    ++bh;
-                }
-                const int s = t % T::STAGES;
-                const int i = w.q_tile(tt);
-                if (t >= T::STAGES &&
-                    !wait_one(b_qdo_empty(s), ((t / T::STAGES) - 1) & 1, abort_flag, prm.st,
-                              SITE_QDO_EMPTY))
-                    break;
+            const int B = prm.BHk / prm.Hk;
+            int g = 0;   // steps loaded so far (all items)
+            int k = 0;   // items whose K/V copy was issued
+            bool ok = true;
+            // Q, dO, -LSE2 and D of global step g (query tile i of query head bh)
+            auto load_step = [&](int i, int bh, int bH0, int b_idx) -> bool {
+                const int s = g % T::STAGES;
+                if (g >= T::STAGES &&
+                    !wait_one(b_qdo_empty(s), ((g / T::STAGES) - 1) & 1, abort_flag, prm.st, SITE_QDO_EMPTY))
+                    return false;
                 const uint32_t bf = b_qdo_full(s);
                 mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
-                const int B = prm.BHk / prm.Hk;
                 for (int blk = 0; blk < 2; ++blk) {
                     const uint32_t dq_ = sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES;
                     const uint32_t ddo = sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES;
@@ -874,10 +878,49 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
                     bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
                 }
+                ++g;
+                return true;
+            };
+            for (int r = 0; ok; ++r) {
+                const int item = item_at(r);
+                if (item == -1) break;
+                if (item < 0) continue;
+                const BwdWork w(prm, item);
+                int tt = 0, bh = w.q_bh0;
+                // the item's first Q/dO stage goes out as soon as a stage is free,
+                // then K and V once the previous item's last products have read them
+                if (w.n_steps > 0 && !load_step(w.q_tile(0), bh, w.bH0, w.b_idx)) {
+                    ok = false;
+                    break;
+                }
+                if (k > 0 && !wait_one(b_kv_empty, (k - 1) & 1, abort_flag, prm.st, SITE_KV_EMPTY)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
+                for (int blk = 0; blk < 2; ++blk) {
+                    if (dbg_tma(sbase + T::OFF_K + blk * T::BLK_BYTES, blk * 64, w.j * kTile, w.hk_idx, w.b_idx,
+                                D, N, prm.Hk, B, 2, 0x2D1))
+                        tma_load_4d(sbase + T::OFF_K + blk * T::BLK_BYTES, &tm_k, b_kv, blk * 64, w.j * kTile,
+                                    w.hk_idx, w.b_idx);
+                    if (dbg_tma(sbase + T::OFF_V + blk * T::BLK_BYTES, blk * 64, w.j * kTile, w.hk_idx, w.b_idx,
+                                D, N, prm.Hk, B, 2, 0x2D2))
+                        tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, w.j * kTile,
+                                    w.hk_idx, w.b_idx);
+                }
+                ++k;
+                for (int t = 1; t < w.n_steps && ok; ++t) {
+                    if (++tt == w.n_qh) {
+                        tt = 0;
+                        ++bh;
+                    }
+                    ok = load_step(w.q_tile(tt), bh, w.bH0, w.b_idx);
+                }
             }
-            wait_drain(b_kv, 0, prm.st, SITE_DRAIN);
-            const int first = t > T::STAGES ? t - T::STAGES : 0;
-            for (int u = first; u < t; ++u)
+            // Let every copy this thread started land before the CTA can exit.
+            if (k > 0) wait_drain(b_kv, (k - 1) & 1, prm.st, SITE_DRAIN);
+            const int first = g > T::STAGES ? g - T::STAGES : 0;
+            for (int u = first; u < g; ++u)
                 wait_drain(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, prm.st, SITE_DRAIN);
         }
     } else if (warp == 13) {
@@ -895,8 +938,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             auto mnmaj = [](uint32_t base, int kk) {
                 return desc_add(sw128_desc_words(base, T::BLK_BYTES, 1024), kk * 16 * 128);
             };
-            auto stage_q = [&](int t) { return sbase + T::OFF_Q + (t % T::STAGES) * T::TILE_BYTES; };
-            auto stage_do = [&](int t) { return sbase + T::OFF_DO + (t % T::STAGES) * T::TILE_BYTES; };
+            auto stage_q = [&](int g) { return sbase + T::OFF_Q + (g % T::STAGES) * T::TILE_BYTES; };
+            auto stage_do = [&](int g) { return sbase + T::OFF_DO + (g % T::STAGES) * T::TILE_BYTES; };
             // S^T or dP^T: M = 128 keys, N = 128 queries, K = d, both operands K-major.
             auto issue_sdp = [&](uint32_t d_tmem, uint32_t a, uint32_t b) {
 #pragma unroll
@@ -921,37 +964,47 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     mma_ss_warp4<false, 0, 128, 256, 384, 0, 128, 256, 384>(
                         tDP, mnmaj(sK, 4 * q), mnmaj(sDS, 4 * q), T::IDESC_DQ, q > 0 ? 1u : 0u);
             };
-            auto run = [&]() -> bool {
-                if (n_steps == 0) return true;
-                if (!wait_warp(b_kv, 0, abort_flag, prm.st, SITE_KV) ||
-                    !wait_warp(b_qdo_full(0), 0, abort_flag, prm.st, SITE_QDO_FULL))
+            int g0 = 0;  // global index of the item's first step
+            int k = 0;   // items started
+            // One item: dkv_full is committed after its last dK product, kv_empty after
+            // its last dQ product (the last reader of K; V's was the last dP^T).
+            auto run_item = [&](int n_steps) -> bool {
+                if (!wait_warp(b_kv, k & 1, abort_flag, prm.st, SITE_KV) ||
+                    !wait_warp(b_qdo_full(g0 % T::STAGES), (g0 / T::STAGES) & 1, abort_flag, prm.st,
+                               SITE_QDO_FULL))
                     return false;
                 tc_fence_after();
-                issue_sdp(tS, sK, stage_q(0));
+                issue_sdp(tS, sK, stage_q(g0));
                 mma_commit_warp(b_s_full);
-                issue_sdp(tDP, sV, stage_do(0));
+                if (g0 > 0) {  // the previous item's last dQ^T has left region dP
+                    if (!wait_warp(b_dq_empty, (g0 - 1) & 1, abort_flag, prm.st, SITE_DQ_EMPTY)) return false;
+                    tc_fence_after();
+                }
+                issue_sdp(tDP, sV, stage_do(g0));
                 mma_commit_warp(b_dp_full);
                 for (int t = 0; t < n_steps; ++t) {
+                    const int g = g0 + t;
                     const uint32_t acc = t > 0 ? 1u : 0u;
-                    if (!wait_warp(b_p_full, t & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                    if (!wait_warp(b_p_full, g & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
                     tc_fence_after();
-                    issue_acc(tDV, tS, stage_do(t), acc);       // dV += P^T(t) dO_t
-                    issue_acc(tDK, tS + 32, stage_q(t), acc);   // dK += dS^T(t) Q_t
-                    mma_commit_warp(b_qdo_empty(t % T::STAGES));
+                    issue_acc(tDV, tS, stage_do(g), acc);       // dV += P^T(t) dO_t
+                    issue_acc(tDK, tS + 32, stage_q(g), acc);   // dK += dS^T(t) Q_t
+                    mma_commit_warp(b_qdo_empty(g % T::STAGES));
                     // dV, dK are final after the last step's products: the epilogue may
                     // start while the last dQ product and its reductions run
                     if (t + 1 == n_steps) mma_commit_warp(b_dkv_full);
                     issue_dq();                                 // dQ^T(t), region dP
                     mma_commit_warp(b_dq_full);
+                    if (t + 1 == n_steps) mma_commit_warp(b_kv_empty);
                     if (t + 1 < n_steps) {
-                        const int u = t + 1;
+                        const int u = g + 1;
                         if (!wait_warp(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, abort_flag, prm.st,
                                        SITE_QDO_FULL))
                             return false;
                         tc_fence_after();
                         issue_sdp(tS, sK, stage_q(u));          // S^T(t+1) over P^T(t), dS^T(t)
                         mma_commit_warp(b_s_full);
-                        if (!wait_warp(b_dq_empty, t & 1, abort_flag, prm.st, SITE_DQ_EMPTY)) return false;
+                        if (!wait_warp(b_dq_empty, g & 1, abort_flag, prm.st, SITE_DQ_EMPTY)) return false;
                         tc_fence_after();
                         issue_sdp(tDP, sV, stage_do(u));        // dP^T(t+1) over dQ^T(t)
                         mma_commit_warp(b_dp_full);
@@ -959,9 +1012,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 return true;
             };
-            // dkv_full is committed after the last dK product (inside run()); when the
-            // loop ended early (a wait gave up) or never ran, commit it here instead
-            if (!run() || n_steps == 0) mma_commit_warp(b_dkv_full);
+            for (int r = 0;; ++r) {
+                const int item = item_at(r);
+                if (item == -1) break;
+                if (item < 0) continue;
+                const BwdWork w(prm, item);
+                if (w.n_steps == 0) {  // nothing sees this key tile: zero dV, dK, release K/V
+                    if (!wait_warp(b_kv, k & 1, abort_flag, prm.st, SITE_KV)) break;
+                    mma_commit_warp(b_dkv_full);
+                    mma_commit_warp(b_kv_empty);
+                } else if (!run_item(w.n_steps)) {
+                    break;
+                }
+                g0 += w.n_steps;
+                ++k;
+            }
             mma_commit_warp(b_done);
             wait_drain(b_done, 0, prm.st, SITE_DRAIN);
         }
@@ -970,7 +1035,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int h = warp >> 2;
         const int wq = warp & 3;
         const int r = wq * 32 + lane;  // key row within the tile
-        const int kv_row = j * kTile + r;
         const uint32_t lane_off = static_cast<uint32_t>(wq * 32) << 16;
         const uint32_t tSh = tmem + T::COL_S + 64 * h + lane_off;
         const uint32_t tDPh = tmem + T::COL_DP + 64 * h + lane_off;
@@ -978,16 +1042,24 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         uint8_t* ds_row = smem + T::OFF_DS + h * T::BLK_BYTES + r * 128;
         const int sw = r & 7;
         bool ok = true;
-        for (int t = 0, tt = 0; t < n_steps; ++t, ++tt) {
-            if (tt == n_qh) tt = 0;
-            const int s = t % T::STAGES;
+        int g = 0;  // global step
+        int k = 0;  // items finished
+        for (int rr = 0; ok; ++rr) {
+        const int item = item_at(rr);
+        if (item == -1) break;
+        if (item < 0) continue;
+        const BwdWork w(prm, item);
+        const int kv_row = w.j * kTile + r;
+        for (int t = 0, tt = 0; t < w.n_steps; ++t, ++tt, ++g) {
+            if (tt == w.n_qh) tt = 0;
+            const int s = g % T::STAGES;
             const int i = w.q_tile(tt);
             const float* nlse2 = reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024) + h * 64;
             const float* dsum = nlse2 + 128;
             // -LSE2_i and D_i arrived with Q_i/dO_i; waiting on that (completed) phase
             // makes the bulk-copied bytes visible to this thread.
-            if (!wait_warp(b_qdo_full(s), (t / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL) ||
-                !wait_warp(b_s_full, t & 1, abort_flag, prm.st, SITE_S_FULL)) {
+            if (!wait_warp(b_qdo_full(s), (g / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL) ||
+                !wait_warp(b_s_full, g & 1, abort_flag, prm.st, SITE_S_FULL)) {
                 ok = false;
                 break;
             }
@@ -1070,7 +1142,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 phase_a(std::false_type{}, C0{});
                 phase_a(std::false_type{}, C1{});
             }
-            if (!wait_warp(b_dp_full, t & 1, abort_flag, prm.st, SITE_DP_FULL)) {
+            if (!wait_warp(b_dp_full, g & 1, abort_flag, prm.st, SITE_DP_FULL)) {
                 ok = false;
                 break;
             }
@@ -1084,14 +1156,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (lane == 0) mbar_arrive(b_p_full);
         }
         // ---- epilogue: warpgroup 0 writes dV, warpgroup 1 writes dK (scaled) ----
-        if (ok && wait_warp(b_dkv_full, 0, abort_flag, prm.st, SITE_DKV)) {
-            tc_fence_after();
+        // Reading dV/dK out of tensor memory here precedes (in this warp's program
+        // order) the arrival that lets the next item's first dV/dK product overwrite
+        // them.
+        if (!ok || !wait_warp(b_dkv_full, k & 1, abort_flag, prm.st, SITE_DKV)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        {
             const bool row_ok = kv_row < N;
             const Strides& ds = h ? prm.dks : prm.dvs;
-            const long long roff = (b_idx * ds.b + hk_idx * ds.h + (row_ok ? kv_row : 0) * ds.n) * 2;
+            const long long roff = (w.b_idx * ds.b + w.hk_idx * ds.h + (row_ok ? kv_row : 0) * ds.n) * 2;
             const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
             uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
             const float f = h ? prm.scale : 1.f;
+            const bool empty = w.n_steps == 0;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t o[32];
@@ -1100,7 +1180,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
-                    pk[e] = n_steps > 0 ? pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f) : 0u;
+                    pk[e] = empty ? 0u : pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f);
                 if (row_ok) {
 #pragma unroll
                     for (int v = 0; v < 4; ++v)
@@ -1109,6 +1189,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
             }
         }
+        ++k;
+        }  // items
     } else {
         // ================= dQ writer (warps 8-11) =================
         // dQ^T(t) sits in region dP with lane = feature, column = query: warp q
@@ -1119,45 +1201,57 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int wq = warp & 3;
         const uint32_t tq = tmem + T::COL_DP + (static_cast<uint32_t>(wq * 32) << 16);
         float* acc_col = prm.dq_acc + static_cast<size_t>(wq * 32 + lane);
-        int tt = 0, bh = q_bh0;
-        for (int t = 0; t < n_steps; ++t, ++tt) {
-            if (tt == n_qh) {
-                tt = 0;
-                ++bh;
-            }
-            const int i = w.q_tile(tt);
-            if (!wait_warp(b_dq_full, t & 1, abort_flag, prm.st, SITE_DQ_FULL)) break;
-            tc_fence_after();
-            uint32_t v0[32], v1[32], v2[32], v3[32];
-            tmem_ld32(tq, v0);
-            tmem_ld32(tq + 32, v1);
-            tmem_ld32(tq + 64, v2);
-            tmem_ld32(tq + 96, v3);
-            tmem_ld_wait(v0);
-            tmem_ld_wait(v1);
-            tmem_ld_wait(v2);
-            tmem_ld_wait(v3);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_dq_empty);
-            float* row0 = acc_col + (static_cast<size_t>(bh) * prm.Npad + i * kTile) * D;
-            // The reductions go out in groups of eight with a short pause between
-            // groups: a burst of 128 per thread right after the drain fills the
-            // memory pipeline that the compute warps' shared-memory loads also use
-            // (whole step 2.55 -> 2.27-2.30 ms at B1 H32 N8192 d128).  The last
-            // step's reductions compete with nothing but the epilogue: no pauses.
-            const bool pace = t + 1 < n_steps;
-            auto send32 = [&](float* rows, const uint32_t (&v)[32]) {
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    red_add_f32(rows + q * D, __uint_as_float(v[q]));
-                    if ((q & 7) == 7 && pace) __nanosleep(kDqPauseNs);
+        bool ok = true;
+        int g = 0;  // global step
+        for (int rr = 0; ok; ++rr) {
+            const int item = item_at(rr);
+            if (item == -1) break;
+            if (item < 0) continue;
+            const BwdWork w(prm, item);
+            const bool last_item = item_at(rr + 1) < 0;
+            int tt = 0, bh = w.q_bh0;
+            for (int t = 0; t < w.n_steps; ++t, ++tt, ++g) {
+                if (tt == w.n_qh) {
+                    tt = 0;
+                    ++bh;
                 }
-            };
-            send32(row0, v0);
-            send32(row0 + 32 * D, v1);
-            send32(row0 + 64 * D, v2);
-            send32(row0 + 96 * D, v3);
+                const int i = w.q_tile(tt);
+                if (!wait_warp(b_dq_full, g & 1, abort_flag, prm.st, SITE_DQ_FULL)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t v0[32], v1[32], v2[32], v3[32];
+                tmem_ld32(tq, v0);
+                tmem_ld32(tq + 32, v1);
+                tmem_ld32(tq + 64, v2);
+                tmem_ld32(tq + 96, v3);
+                tmem_ld_wait(v0);
+                tmem_ld_wait(v1);
+                tmem_ld_wait(v2);
+                tmem_ld_wait(v3);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_dq_empty);
+                float* row0 = acc_col + (static_cast<size_t>(bh) * prm.Npad + i * kTile) * D;
+                // The reductions go out in groups of eight with a short pause between
+                // groups: a burst of 128 per thread right after the drain fills the
+                // memory pipeline that the compute warps' shared-memory loads also use
+                // (whole step 2.55 -> 2.27-2.30 ms at B1 H32 N8192 d128).  The CTA's
+                // last step competes with nothing but the epilogue: no pauses.
+                const bool pace = !(last_item && t + 1 == w.n_steps);
+                auto send32 = [&](float* rows, const uint32_t (&v)[32]) {
+#pragma unroll
+                    for (int q = 0; q < 32; ++q) {
+                        red_add_f32(rows + q * D, __uint_as_float(v[q]));
+                        if ((q & 7) == 7 && pace) __nanosleep(kDqPauseNs);
+                    }
+                };
+                send32(row0, v0);
+                send32(row0 + 32 * D, v1);
+                send32(row0 + 64 * D, v2);
+                send32(row0 + 96 * D, v3);
+            }
         }
     }
 
@@ -1216,7 +1310,14 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
         static const cudaError_t attr = cudaFuncSetAttribute(
             bwd_main_full_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
         if (attr != cudaSuccess) return attr;
-        const long long grid = static_cast<long long>(p.BHk) * p.n_kv;
+        // persistent: one CTA per SM (shared memory admits one), items in snake order
+        long long grid = static_cast<long long>(p.BHk) * p.n_kv;
+        int dev = 0, sms = 0;
+        cudaError_t e = cudaGetDevice(&dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (sms < grid) grid = sms;
+        if (grid < 1) return cudaSuccess;
         const cudaError_t dbg = dbg_set_word(p.st.word, stream);
         if (dbg != cudaSuccess) return dbg;
         bwd_main_full_kernel<<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
