@@ -735,8 +735,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // while dP^T(t+1) executes, and only the dS^T pass is exposed.  The tensor
 // pipe executes in issue order, so a product that overwrites a region is
 // issued after the last product that reads it.
+// The per-query terms -LSE log2 e (of the exponent) and -D (of dS) are not
+// loaded by the compute warps: each enters S^T or dP^T through one more K = 16
+// product against a tile of their bf16 parts, so S^T holds S^T - LSE log2 e / cs
+// and dP^T holds dP^T - D (the per-column broadcast loads they replace shared
+// the memory pipeline with the dQ reductions).
 // Warps 0-3 / 4-7: compute for query columns 0-63 / 64-127 of the tile (one
-// thread per key row); warps 8-11: dQ writer; warp 12: TMA; warp 13: MMA.
+// thread per key row); warps 8-11: dQ writer; warp 12: TMA and the per-query
+// terms; warp 13: MMA.
 struct BwdFullTraits {
     static constexpr int D = 128;
     static constexpr int BLK_BYTES = kTile * 128;        // one [128 rows x 128 B] block
@@ -749,11 +755,16 @@ struct BwdFullTraits {
     static constexpr int OFF_Q = OFF_V + TILE_BYTES;            // + stage * TILE_BYTES
     static constexpr int OFF_DO = OFF_Q + STAGES * TILE_BYTES;  // + stage * TILE_BYTES
     static constexpr int OFF_DS = OFF_DO + STAGES * TILE_BYTES;
-    static constexpr int OFF_VEC = OFF_DS + DS_BYTES;           // -LSE2[s], D[s]: 512 B each
-    static constexpr int OFF_BAR = OFF_VEC + STAGES * 2 * 512;
+    // The per-query terms of the exponent (-LSE log2 e / cs) and of dS (-D) enter
+    // S^T and dP^T as one more K = 16 product each: A = a row of ones over the
+    // term's parts (the same 8 rows for every row group), B = each query's parts
+    // (written per step by the producer warp).
+    static constexpr int OFF_AUG_A = OFF_DS + DS_BYTES;         // 2 core matrices, 8 x 16 B each
+    static constexpr int OFF_AUG_B = OFF_AUG_A + 2 * 128;       // [128 queries][8 bf16]
+    static constexpr int OFF_BAR = OFF_AUG_B + kTile * 16;
     // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_full, dq_full,
-    //           dq_empty, dkv_full, done, kv_empty
-    static constexpr int NBARS = 1 + 2 * STAGES + 8;
+    //           dq_empty, dkv_full, done, kv_empty, aug_full
+    static constexpr int NBARS = 1 + 2 * STAGES + 9;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
     static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, kTile, false, false);
@@ -762,7 +773,20 @@ struct BwdFullTraits {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C };
+enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C, SITE_AUG_FULL = 0x20D };
+
+// v as hi + mid + lo, each rounded to bf16 (hi + mid + lo = v to about 2^-24
+// relative: each remainder is exact in fp32), returned halved (exact) and
+// packed as the bf16 words (hi/2 | mid/2 << 16, lo/2).
+__device__ __forceinline__ uint2 split3_half_bf16(float v) {
+    const uint32_t hb = pack_bf16x2(v, 0.f);
+    const float r1 = v - __uint_as_float(hb << 16);
+    const uint32_t mb = pack_bf16x2(r1, 0.f);
+    const float r2 = r1 - __uint_as_float(mb << 16);
+    const uint32_t lb = pack_bf16x2(r2, 0.f);
+    const uint32_t h2 = pack_bf16x2(0.5f * __uint_as_float(hb << 16), 0.5f * __uint_as_float(mb << 16));
+    return make_uint2(h2, pack_bf16x2(0.5f * __uint_as_float(lb << 16), 0.f));
+}
 
 // Pause of the dQ writer between groups of eight reductions (see the writer).
 constexpr unsigned kDqPauseNs = 60;
@@ -793,6 +817,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t b_dkv_full = b_dq_empty + 8u;
     const uint32_t b_done = b_dkv_full + 8u;
     const uint32_t b_kv_empty = b_done + 8u;                     // an item's K, V read for the last time
+    const uint32_t b_aug_full = b_kv_empty + 8u;                 // per-query terms of the next step written
 
     if ((sbase & 1023u) != 0) {
         if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FE);
@@ -830,6 +855,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(b_dq_empty, 4);  // one arrival per dQ-writer warp
         mbar_init(b_dkv_full, 1);
         mbar_init(b_done, 1);
+        mbar_init(b_aug_full, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -843,6 +869,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         tma_prefetch_map(&tm_v);
         tma_prefetch_map(&tm_do);
     }
+    if (warp == 12 && lane < 16) {
+        // the constant A tile of the per-query products: row i of core matrix 0 (the
+        // S^T term, ones over elements 0-2) and of core matrix 1 (the dP^T term,
+        // ones over elements 4-6)
+        const uint32_t one2 = 0x3F803F80u, one1 = 0x00003F80u;  // bf16 1.0 pairs
+        *reinterpret_cast<uint4*>(smem + T::OFF_AUG_A + lane * 16) =
+            lane < 8 ? make_uint4(one2, one1, 0u, 0u) : make_uint4(0u, 0u, one2, one1);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -851,20 +886,80 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // Steps are counted over all of the CTA's items (g): the Q/dO stages and the
     // per-step barriers run on through item boundaries.
     if (warp == 12) {
-        // ================= TMA producer =================
-        if (lane == 0) {
-            const int B = prm.BHk / prm.Hk;
-            int g = 0;   // steps loaded so far (all items)
-            int k = 0;   // items whose K/V copy was issued
-            bool ok = true;
-            // Q, dO, -LSE2 and D of global step g (query tile i of query head bh)
-            auto load_step = [&](int i, int bh, int bH0, int b_idx) -> bool {
-                const int s = g % T::STAGES;
-                if (g >= T::STAGES &&
-                    !wait_one(b_qdo_empty(s), ((g / T::STAGES) - 1) & 1, abort_flag, prm.st, SITE_QDO_EMPTY))
-                    return false;
+        // ================= TMA producer and per-query terms =================
+        // The whole warp runs the loop (lane 0 issues the copies).  Besides Q, dO,
+        // K and V it writes, per step, the B tile of the per-query products: row q
+        // holds halves of the three bf16 parts of -LSE log2 e / cs (the S^T term:
+        // P^T = 2^(cs (S^T - LSE log2 e / cs))) and of -D (the dP^T term); lane l
+        // owns rows l + 32 m.  The raw values are loaded a step ahead of the step's
+        // copies and written a step after them, once dP^T of the previous step (the
+        // last reader of the single tile) has completed; aug_full publishes them to
+        // the MMA warp before that step's S^T.
+        const int B = prm.BHk / prm.Hk;
+        const float rcs = 1.f / prm.cs;
+        int g = 0;   // steps loaded so far (all items)
+        int k = 0;   // items whose K/V copy was issued
+        bool ok = true;
+        float raw_l[4], raw_d[4];  // -LSE log2 e and D of step `pend`, rows lane + 32 m
+        float nxt_l[4], nxt_d[4];  // the same for step pend + 1 (in flight)
+        int pend = -1;             // step whose terms are loaded but not yet written (-1: none)
+        auto fetch = [&](int bh, int i) {  // step (query head bh, tile i) into nxt (bh < 0: none)
+            if (bh < 0) return;
+            const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile + lane;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                nxt_l[m] = prm.lse2[vrow + 32 * m];
+                nxt_d[m] = prm.dsum[vrow + 32 * m];
+            }
+        };
+        // (query head, tile) of the first step of the CTA's items from round rr on
+        auto first_step = [&](int rr, int& bh, int& tile) {
+            bh = -1;
+            tile = 0;
+            for (;; ++rr) {
+                const int item = item_at(rr);
+                if (item == -1) return;
+                if (item < 0) continue;
+                const BwdWork w(prm, item);
+                if (w.n_steps > 0) {
+                    bh = w.q_bh0;
+                    tile = w.q_tile(0);
+                    return;
+                }
+            }
+        };
+        auto write_terms = [&]() -> bool {
+            if (pend < 0) return true;
+            if (pend > 0 && !wait_warp(b_dp_full, (pend - 1) & 1, abort_flag, prm.st, SITE_DP_FULL)) return false;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                float vl = raw_l[m] * rcs;
+                // -inf on padding rows: a large finite negative value makes P^T zero
+                // there; +inf (a row that sees no key) only meets masked entries
+                if (!(vl >= -1e30f)) vl = -1e30f;
+                if (!(vl <= 1e30f)) vl = 0.f;
+                const uint2 a = split3_half_bf16(vl), b = split3_half_bf16(-raw_d[m]);
+                *reinterpret_cast<uint4*>(smem + T::OFF_AUG_B + (lane + 32 * m) * 16) =
+                    make_uint4(a.x, a.y, b.x, b.y);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_aug_full);
+            pend = -1;
+            return true;
+        };
+        // Q and dO of global step g (query tile i of query head bh); the previous
+        // step's terms are written first, and those of the step after this one
+        // (query head nbh, tile ni; nbh < 0: none) are fetched
+        auto load_step = [&](int i, int bh, int bH0, int b_idx, int nbh, int ni) -> bool {
+            if (!write_terms()) return false;
+            const int s = g % T::STAGES;
+            if (g >= T::STAGES &&
+                !wait_warp(b_qdo_empty(s), ((g / T::STAGES) - 1) & 1, abort_flag, prm.st, SITE_QDO_EMPTY))
+                return false;
+            if (lane == 0) {
                 const uint32_t bf = b_qdo_full(s);
-                mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES + 1024);
+                mbar_arrive_expect_tx(bf, 2 * T::TILE_BYTES);
                 for (int blk = 0; blk < 2; ++blk) {
                     const uint32_t dq_ = sbase + T::OFF_Q + s * T::TILE_BYTES + blk * T::BLK_BYTES;
                     const uint32_t ddo = sbase + T::OFF_DO + s * T::TILE_BYTES + blk * T::BLK_BYTES;
@@ -873,30 +968,55 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (dbg_tma(ddo, blk * 64, i * kTile, bh - bH0, b_idx, D, N, prm.H, B, 2, 0x2D4))
                         tma_load_4d(ddo, &tm_do, bf, blk * 64, i * kTile, bh - bH0, b_idx);
                 }
-                const size_t vrow = static_cast<size_t>(bh) * prm.Npad + i * kTile;
-                if (dbg_ok(vrow + kTile <= static_cast<size_t>(B) * prm.H * prm.Npad, 0x2D5)) {
-                    bulk_load(sbase + T::OFF_VEC + s * 1024, prm.lse2 + vrow, 512, bf);
-                    bulk_load(sbase + T::OFF_VEC + s * 1024 + 512, prm.dsum + vrow, 512, bf);
+            }
+            __syncwarp();
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                raw_l[m] = nxt_l[m];
+                raw_d[m] = nxt_d[m];
+            }
+            fetch(nbh, ni);
+            pend = g;
+            ++g;
+            return true;
+        };
+        {
+            int bh0, tile0;
+            first_step(0, bh0, tile0);
+            fetch(bh0, tile0);
+        }
+        for (int r = 0; ok; ++r) {
+            const int item = item_at(r);
+            if (item == -1) break;
+            if (item < 0) continue;
+            const BwdWork w(prm, item);
+            int nx_bh, nx_tile;  // first step of the next item with steps
+            first_step(r + 1, nx_bh, nx_tile);
+            int tt = 0, bh = w.q_bh0;
+            // (query head, tile) of the step after step t of this item
+            auto after = [&](int t, int& nbh, int& ni) {
+                if (t + 1 >= w.n_steps) {
+                    nbh = nx_bh;
+                    ni = nx_tile;
+                } else {
+                    const bool wrap = tt + 1 == w.n_qh;
+                    nbh = wrap ? bh + 1 : bh;
+                    ni = w.q_tile(wrap ? 0 : tt + 1);
                 }
-                ++g;
-                return true;
             };
-            for (int r = 0; ok; ++r) {
-                const int item = item_at(r);
-                if (item == -1) break;
-                if (item < 0) continue;
-                const BwdWork w(prm, item);
-                int tt = 0, bh = w.q_bh0;
-                // the item's first Q/dO stage goes out as soon as a stage is free,
-                // then K and V once the previous item's last products have read them
-                if (w.n_steps > 0 && !load_step(w.q_tile(0), bh, w.bH0, w.b_idx)) {
-                    ok = false;
-                    break;
-                }
-                if (k > 0 && !wait_one(b_kv_empty, (k - 1) & 1, abort_flag, prm.st, SITE_KV_EMPTY)) {
-                    ok = false;
-                    break;
-                }
+            int nbh, ni;
+            // the item's first Q/dO stage goes out as soon as a stage is free,
+            // then K and V once the previous item's last products have read them
+            after(0, nbh, ni);
+            if (w.n_steps > 0 && !load_step(w.q_tile(0), bh, w.bH0, w.b_idx, nbh, ni)) {
+                ok = false;
+                break;
+            }
+            if (k > 0 && !wait_warp(b_kv_empty, (k - 1) & 1, abort_flag, prm.st, SITE_KV_EMPTY)) {
+                ok = false;
+                break;
+            }
+            if (lane == 0) {
                 mbar_arrive_expect_tx(b_kv, 2 * T::TILE_BYTES);
                 for (int blk = 0; blk < 2; ++blk) {
                     if (dbg_tma(sbase + T::OFF_K + blk * T::BLK_BYTES, blk * 64, w.j * kTile, w.hk_idx, w.b_idx,
@@ -908,21 +1028,27 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         tma_load_4d(sbase + T::OFF_V + blk * T::BLK_BYTES, &tm_v, b_kv, blk * 64, w.j * kTile,
                                     w.hk_idx, w.b_idx);
                 }
-                ++k;
-                for (int t = 1; t < w.n_steps && ok; ++t) {
-                    if (++tt == w.n_qh) {
-                        tt = 0;
-                        ++bh;
-                    }
-                    ok = load_step(w.q_tile(tt), bh, w.bH0, w.b_idx);
-                }
             }
-            // Let every copy this thread started land before the CTA can exit.
+            __syncwarp();
+            ++k;
+            for (int t = 1; t < w.n_steps && ok; ++t) {
+                if (++tt == w.n_qh) {
+                    tt = 0;
+                    ++bh;
+                }
+                after(t, nbh, ni);
+                ok = load_step(w.q_tile(tt), bh, w.bH0, w.b_idx, nbh, ni);
+            }
+        }
+        if (ok) write_terms();  // the last step's terms
+        // Let every copy this warp started land before the CTA can exit.
+        if (lane == 0) {
             if (k > 0) wait_drain(b_kv, (k - 1) & 1, prm.st, SITE_DRAIN);
             const int first = g > T::STAGES ? g - T::STAGES : 0;
             for (int u = first; u < g; ++u)
                 wait_drain(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, prm.st, SITE_DRAIN);
         }
+        __syncwarp();
     } else if (warp == 13) {
         // ================= MMA issuer =================
         __syncwarp();
@@ -940,12 +1066,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             };
             auto stage_q = [&](int g) { return sbase + T::OFF_Q + (g % T::STAGES) * T::TILE_BYTES; };
             auto stage_do = [&](int g) { return sbase + T::OFF_DO + (g % T::STAGES) * T::TILE_BYTES; };
-            // S^T or dP^T: M = 128 keys, N = 128 queries, K = d, both operands K-major.
-            auto issue_sdp = [&](uint32_t d_tmem, uint32_t a, uint32_t b) {
+            // The per-query term as one more product: A (no swizzle, both steps 0)
+            // repeats one core matrix of ones over the term's parts in every row and
+            // in both halves of K = 16, B (no swizzle, K step 0) repeats each query's
+            // parts, so the product adds twice the sum of the stored half-parts.
+            const SmemDesc aug_b = noswz_desc_words(sbase + T::OFF_AUG_B, 0, 128);
+            const SmemDesc aug_s = noswz_desc_words(sbase + T::OFF_AUG_A, 0, 0);
+            const SmemDesc aug_dp = noswz_desc_words(sbase + T::OFF_AUG_A + 128, 0, 0);
+            // S^T or dP^T: M = 128 keys, N = 128 queries, K = d, both operands K-major,
+            // plus the per-query term.
+            auto issue_sdp = [&](uint32_t d_tmem, uint32_t a, uint32_t b, SmemDesc aug) {
 #pragma unroll
                 for (int q = 0; q < D / 64; ++q)
                     mma_ss_warp4<false, 0, 2, 4, 6, 0, 2, 4, 6>(d_tmem, kmaj(a, 4 * q), kmaj(b, 4 * q),
                                                                 T::IDESC_SDP, q > 0 ? 1u : 0u);
+                mma_ss_warp1_acc(d_tmem, aug, aug_b, T::IDESC_SDP);
             };
             // dV or dK += A B: A = packed bf16 in tensor memory (queries 0-63 at +0,
             // 64-127 at +64: each compute warpgroup packs over its own columns), B
@@ -971,16 +1106,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             auto run_item = [&](int n_steps) -> bool {
                 if (!wait_warp(b_kv, k & 1, abort_flag, prm.st, SITE_KV) ||
                     !wait_warp(b_qdo_full(g0 % T::STAGES), (g0 / T::STAGES) & 1, abort_flag, prm.st,
-                               SITE_QDO_FULL))
+                               SITE_QDO_FULL) ||
+                    !wait_warp(b_aug_full, g0 & 1, abort_flag, prm.st, SITE_AUG_FULL))
                     return false;
                 tc_fence_after();
-                issue_sdp(tS, sK, stage_q(g0));
+                issue_sdp(tS, sK, stage_q(g0), aug_s);
                 mma_commit_warp(b_s_full);
                 if (g0 > 0) {  // the previous item's last dQ^T has left region dP
                     if (!wait_warp(b_dq_empty, (g0 - 1) & 1, abort_flag, prm.st, SITE_DQ_EMPTY)) return false;
                     tc_fence_after();
                 }
-                issue_sdp(tDP, sV, stage_do(g0));
+                issue_sdp(tDP, sV, stage_do(g0), aug_dp);
                 mma_commit_warp(b_dp_full);
                 for (int t = 0; t < n_steps; ++t) {
                     const int g = g0 + t;
@@ -999,14 +1135,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (t + 1 < n_steps) {
                         const int u = g + 1;
                         if (!wait_warp(b_qdo_full(u % T::STAGES), (u / T::STAGES) & 1, abort_flag, prm.st,
-                                       SITE_QDO_FULL))
+                                       SITE_QDO_FULL) ||
+                            !wait_warp(b_aug_full, u & 1, abort_flag, prm.st, SITE_AUG_FULL))
                             return false;
                         tc_fence_after();
-                        issue_sdp(tS, sK, stage_q(u));          // S^T(t+1) over P^T(t), dS^T(t)
+                        issue_sdp(tS, sK, stage_q(u), aug_s);   // S^T(t+1) over P^T(t), dS^T(t)
                         mma_commit_warp(b_s_full);
                         if (!wait_warp(b_dq_empty, g & 1, abort_flag, prm.st, SITE_DQ_EMPTY)) return false;
                         tc_fence_after();
-                        issue_sdp(tDP, sV, stage_do(u));        // dP^T(t+1) over dQ^T(t)
+                        issue_sdp(tDP, sV, stage_do(u), aug_dp);  // dP^T(t+1) over dQ^T(t)
                         mma_commit_warp(b_dp_full);
                     }
                 }
@@ -1052,14 +1189,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int kv_row = w.j * kTile + r;
         for (int t = 0, tt = 0; t < w.n_steps; ++t, ++tt, ++g) {
             if (tt == w.n_qh) tt = 0;
-            const int s = g % T::STAGES;
             const int i = w.q_tile(tt);
-            const float* nlse2 = reinterpret_cast<const float*>(smem + T::OFF_VEC + s * 1024) + h * 64;
-            const float* dsum = nlse2 + 128;
-            // -LSE2_i and D_i arrived with Q_i/dO_i; waiting on that (completed) phase
-            // makes the bulk-copied bytes visible to this thread.
-            if (!wait_warp(b_qdo_full(s), (g / T::STAGES) & 1, abort_flag, prm.st, SITE_QDO_FULL) ||
-                !wait_warp(b_s_full, g & 1, abort_flag, prm.st, SITE_S_FULL)) {
+            if (!wait_warp(b_s_full, g & 1, abort_flag, prm.st, SITE_S_FULL)) {
                 ok = false;
                 break;
             }
@@ -1071,8 +1202,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int cmax = prm.win_left < 0 ? 2 * kTile : kv_row + prm.win_left - qc0;
             const bool masked = __any_sync(0xffffffffu, cmin > 0 || cmax < 63);
             float p[64];  // P^T of this thread's key row and the warpgroup's 64 queries
-            // Phase A: P^T = 2^(S^T cs - LSE log2 e); packed bf16 over the S^T columns
-            // already read (the A operand of dV), fp32 kept for dS^T.
+            // Phase A: P^T = 2^(cs (S^T - LSE log2 e / cs)), the query term already in
+            // S^T; packed bf16 over the S^T columns already read (the A operand of
+            // dV), fp32 kept for dS^T.
             auto phase_a = [&](auto masked_tag, auto cc_tag) {
                 constexpr bool kMasked = decltype(masked_tag)::value;
                 constexpr int cc = decltype(cc_tag)::value;
@@ -1081,31 +1213,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld32(tSh + c0, sv);
                 tmem_ld_wait(sv);
                 uint32_t pk[16];
-                const float4* nl4 = reinterpret_cast<const float4*>(nlse2 + c0);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 nl = nl4[e / 4];  // same address in every lane: broadcast
-                    const float nlv[4] = {nl.x, nl.y, nl.z, nl.w};
-#pragma unroll
-                    for (int h2 = 0; h2 < 4; h2 += 2) {
-                        const int c = c0 + e + h2;
-                        float x0, x1;
-                        ffma2(x0, x1, u2f(sv[e + h2]), u2f(sv[e + h2 + 1]), cs, cs, nlv[h2], nlv[h2 + 1]);
-                        float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-                        if constexpr (kMasked) {
-                            if (c < cmin || c > cmax) p0 = 0.f;
-                            if (c + 1 < cmin || c + 1 > cmax) p1 = 0.f;
-                        }
-                        p[c] = p0;
-                        p[c + 1] = p1;
-                        pk[(e + h2) / 2] = pack_bf16x2(p0, p1);
+                for (int e = 0; e < 32; e += 2) {
+                    const int c = c0 + e;
+                    float x0, x1;
+                    fmul2(x0, x1, u2f(sv[e]), u2f(sv[e + 1]), cs, cs);
+                    float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+                    if constexpr (kMasked) {
+                        if (c < cmin || c > cmax) p0 = 0.f;
+                        if (c + 1 < cmin || c + 1 > cmax) p1 = 0.f;
                     }
+                    p[c] = p0;
+                    p[c + 1] = p1;
+                    pk[e / 2] = pack_bf16x2(p0, p1);
                 }
                 tmem_st16(tSh + 16 * cc, pk);
             };
-            // Phase B: dS^T = P^T (dP^T - D); packed bf16 over the second 32 of this
-            // warpgroup's S^T columns (read in phase A; the A operand of dK) and into
-            // shared memory with 128-byte swizzle (the B operand of dQ^T, MN-major).
+            // Phase B: dS^T = P^T (dP^T - D), the -D term already in dP^T; packed bf16
+            // over the second 32 of this warpgroup's S^T columns (read in phase A; the
+            // A operand of dK) and into shared memory with 128-byte swizzle (the B
+            // operand of dQ^T, MN-major).
             auto phase_b = [&](auto cc_tag) {
                 constexpr int cc = decltype(cc_tag)::value;
                 constexpr int c0 = cc * 32;
@@ -1113,19 +1240,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld32(tDPh + c0, dp);
                 tmem_ld_wait(dp);
                 uint32_t dsw[16];
-                const float4* ds4 = reinterpret_cast<const float4*>(dsum + c0);
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    const float4 dd = ds4[e / 4];
-                    const float ddv[4] = {dd.x, dd.y, dd.z, dd.w};
-#pragma unroll
-                    for (int h2 = 0; h2 < 4; h2 += 2) {
-                        const int c = c0 + e + h2;
-                        float t0, t1, d0, d1;
-                        fsub2(t0, t1, u2f(dp[e + h2]), u2f(dp[e + h2 + 1]), ddv[h2], ddv[h2 + 1]);
-                        fmul2(d0, d1, p[c], p[c + 1], t0, t1);
-                        dsw[(e + h2) / 2] = pack_bf16x2(d0, d1);
-                    }
+                for (int e = 0; e < 32; e += 2) {
+                    float d0, d1;
+                    fmul2(d0, d1, p[c0 + e], p[c0 + e + 1], u2f(dp[e]), u2f(dp[e + 1]));
+                    dsw[e / 2] = pack_bf16x2(d0, d1);
                 }
                 tmem_st16(tSh + 32 + 16 * cc, dsw);
 #pragma unroll

@@ -370,6 +370,21 @@ __device__ __forceinline__ SmemDesc desc_add(SmemDesc d, uint32_t byte_offset) {
     return SmemDesc{d.lo + (byte_offset >> 4), d.hi};
 }
 
+// Descriptor of a K-major operand without swizzle (swizzle mode 0): the
+// operand is made of core matrices of 8 rows x 16 bytes (8 bf16 of K), each
+// stored contiguously (row i at +16 i); LBO is the byte step between core
+// matrices adjacent in K and SBO the step between adjacent 8-row groups of M/N.
+// Any step, zero included, is a valid descriptor: a zero SBO makes every
+// 8-row group read the same eight rows.
+__device__ __forceinline__ SmemDesc noswz_desc_words(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;
+    return SmemDesc{static_cast<uint32_t>(d), static_cast<uint32_t>(d >> 32)};
+}
+
 // Warp-wide forms: every lane of a converged warp executes the call with the
 // same (warp-uniform) operands and one lane, chosen by elect.sync, issues the
 // instructions.  Keeping the issuing loop on the whole warp lets the compiler
@@ -467,6 +482,20 @@ __device__ __forceinline__ void mma_ts_warp4(uint32_t d_tmem, uint32_t a_tmem, S
             "n"(OA0), "n"(OA1), "n"(OA2), "n"(OA3), "n"(OB0), "n"(OB1), "n"(OB2), "n"(OB3)
             : "memory");
     }
+}
+
+// One bf16 product (kind::f16, both operands in shared memory) from the
+// elected lane of a converged warp; it accumulates into D.
+__device__ __forceinline__ void mma_ss_warp1_acc(uint32_t d_tmem, SmemDesc a, SmemDesc b, uint32_t idesc) {
+    if (!dbg_ok((d_tmem >> 16) == 0 && (d_tmem & 0xFFFFu) + ((idesc >> 17) & 0x3Fu) * 8u <= 512u, 0xD06))
+        return;
+    asm volatile(
+        "{\n\t.reg .pred e, t;\n\t.reg .b64 da, db;\n\t"
+        "setp.eq.b32 t, %5, %5;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "mov.b64 da, {%1, %2};\n\tmov.b64 db, {%3, %4};\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %5, t;\n\t}"
+        ::"r"(d_tmem), "r"(a.lo), "r"(a.hi), "r"(b.lo), "r"(b.hi), "r"(idesc)
+        : "memory");
 }
 
 // Arrive (once) on `bar` when every tcgen05.mma issued so far by the issuing
