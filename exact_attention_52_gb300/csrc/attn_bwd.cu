@@ -728,11 +728,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // it packs P^T over the first 32 of its S columns and dS^T over the other 32,
 // so both A operands sit in region S and region dP is free as soon as dP^T has
 // been read.  Issue order of step t:
-//   dV(t), dK(t), dQ^T(t), S^T(t+1), [dQ^T(t) drained], dP^T(t+1),
-//   [P^T(t+1), dS^T(t+1) formed], dV(t+1) ...
+//   [P^T(t) formed] dV(t), [dS^T(t) formed] dK(t), dQ^T(t), S^T(t+1),
+//   [dQ^T(t) drained], dP^T(t+1), [P^T(t+1) formed] dV(t+1) ...
 // The dQ writer takes dQ^T(t) out of tensor memory while S^T(t+1) executes, so
 // the drain costs the tensor pipe nothing; the exponentials of step t+1 run
-// while dP^T(t+1) executes, and only the dS^T pass is exposed.  The tensor
+// while dP^T(t+1) executes and the dS^T pass while dV(t+1) does.  The tensor
 // pipe executes in issue order, so a product that overwrites a region is
 // issued after the last product that reads it.
 // The per-query terms -LSE log2 e (of the exponent) and -D (of dS) are not
@@ -763,8 +763,8 @@ struct BwdFullTraits {
     static constexpr int OFF_AUG_B = OFF_AUG_A + 2 * 128;       // [128 queries][8 bf16]
     static constexpr int OFF_BAR = OFF_AUG_B + kTile * 16;
     // barriers: kv_full, qdo_full[2], qdo_empty[2], s_full, dp_full, p_full, dq_full,
-    //           dq_empty, dkv_full, done, kv_empty, aug_full
-    static constexpr int NBARS = 1 + 2 * STAGES + 9;
+    //           dq_empty, dkv_full, done, kv_empty, aug_full, pa_full
+    static constexpr int NBARS = 1 + 2 * STAGES + 10;
     static constexpr int SMEM_BYTES = OFF_BAR + NBARS * 8 + 16;
     static constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 384;
     static constexpr uint32_t IDESC_SDP = make_idesc(kFmtBF16, kTile, kTile, false, false);
@@ -773,7 +773,7 @@ struct BwdFullTraits {
     static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 };
 
-enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C, SITE_AUG_FULL = 0x20D };
+enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C, SITE_AUG_FULL = 0x20D, SITE_PA_FULL = 0x20E };
 
 // v as hi + mid + lo, each rounded to bf16 (hi + mid + lo = v to about 2^-24
 // relative: each remainder is exact in fp32), returned halved (exact) and
@@ -818,6 +818,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     const uint32_t b_done = b_dkv_full + 8u;
     const uint32_t b_kv_empty = b_done + 8u;                     // an item's K, V read for the last time
     const uint32_t b_aug_full = b_kv_empty + 8u;                 // per-query terms of the next step written
+    const uint32_t b_pa_full = b_aug_full + 8u;                  // P^T(t) formed (dS^T(t) not yet)
 
     if ((sbase & 1023u) != 0) {
         if (threadIdx.x == 0) record_device_error(prm.st, ATTN_DEVERR_SMEM_ALIGN, 0x2FE);
@@ -851,6 +852,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(b_s_full, 1);
         mbar_init(b_dp_full, 1);
         mbar_init(b_p_full, 8);    // one arrival per compute warp
+        mbar_init(b_pa_full, 8);
         mbar_init(b_dq_full, 1);
         mbar_init(b_dq_empty, 4);  // one arrival per dQ-writer warp
         mbar_init(b_dkv_full, 1);
@@ -1121,9 +1123,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int t = 0; t < n_steps; ++t) {
                     const int g = g0 + t;
                     const uint32_t acc = t > 0 ? 1u : 0u;
-                    if (!wait_warp(b_p_full, g & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                    // dV(t) as soon as P^T(t) is formed: it runs during the dS^T pass
+                    if (!wait_warp(b_pa_full, g & 1, abort_flag, prm.st, SITE_PA_FULL)) return false;
                     tc_fence_after();
                     issue_acc(tDV, tS, stage_do(g), acc);       // dV += P^T(t) dO_t
+                    if (!wait_warp(b_p_full, g & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
+                    tc_fence_after();
                     issue_acc(tDK, tS + 32, stage_q(g), acc);   // dK += dS^T(t) Q_t
                     mma_commit_warp(b_qdo_empty(g % T::STAGES));
                     // dV, dK are final after the last step's products: the epilogue may
@@ -1261,6 +1266,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 phase_a(std::false_type{}, C0{});
                 phase_a(std::false_type{}, C1{});
             }
+            // P^T(t) is complete in tensor memory: dV(t) may start
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_pa_full);
             if (!wait_warp(b_dp_full, g & 1, abort_flag, prm.st, SITE_DP_FULL)) {
                 ok = false;
                 break;
