@@ -1,12 +1,14 @@
 """Backward parity: dQ, dK, dV from the CUDA path vs the fp64 oracle (relative
 Frobenius error per tensor), on tiles with ragged tails, both masks."""
 
+import dataclasses
+
 import numpy as np
 import pytest
 
 import oracle
 from exact_attention_52_gb300 import api
-from exact_attention_52_gb300.inputs import make_inputs
+from exact_attention_52_gb300.inputs import f32_to_bf16_bits, make_inputs
 
 from .helpers import (TOL_GRAD_RELFRO, bf16_to_device, decoded, device_bf16_to_f64, grad_rel_err,
                       rel_fro)
@@ -52,3 +54,25 @@ def test_bwd_dk_dv_deterministic_dq_within_tolerance():
     b = run_fwd_bwd(inp, True)
     assert np.array_equal(a[1], b[1]) and np.array_equal(a[2], b[2])
     assert rel_fro(a[0], b[0]) <= 1e-3  # fp32 reduction order only
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("scale_mult", [1e-2, 1.0, 8.0])
+def test_bwd_score_scales_and_large_dout(scale_mult, causal):
+    """For d = 128 the per-query terms -LSE log2 e / c and -D reach S^T and dP^T
+    through one more tensor-core product each, as three bf16 parts of the term.
+    Scales from 0.01 to 8 times 1/sqrt(d) move that term from about -6500 to
+    about -30 (nearly uniform to sharply peaked P), and a dO multiplied by 64
+    (exact in bf16) makes D large against dP - D."""
+    d, N = 128, 300
+    inp = make_inputs(1, 2, N, d, seed=4242 + int(causal), with_grad=True)
+    big = dataclasses.replace(inp, do_bits=f32_to_bf16_bits(decoded(inp)[3].astype(np.float32) * 64.0))
+    scale = scale_mult / np.sqrt(d)
+    for case in (inp, big):
+        got = run_fwd_bwd(case, causal, scale=scale)
+        q, k, v, do = decoded(case)
+        ref = oracle.backward(q, k, v, do, scale, causal)
+        for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+            assert np.all(np.isfinite(g)), name
+            err = grad_rel_err(g, r)
+            assert err <= TOL_GRAD_RELFRO, (name, err)
