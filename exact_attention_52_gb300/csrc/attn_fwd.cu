@@ -227,29 +227,53 @@ __global__ void __launch_bounds__(320, 1)
                 if (item == -1) break;
                 if (item < 0) continue;
                 const Item it = item_info(item);
-                // K_j, V_j of the item's key tile j into the ring
-                auto load_kv = [&](int j) -> bool {
-                    for (int t = 0; t < 2; ++t, ++idx) {  // t = 0: K_j, t = 1: V_j
-                        const int slot = idx % T::KV_SLOTS;
-                        const int round = idx / T::KV_SLOTS;
-                        if (round > 0 &&
-                            !wait_one(b_kv_empty(slot), (round - 1) & 1, abort_flag, prm.st, SITE_KV_EMPTY))
-                            return false;
-                        mbar_arrive_expect_tx(b_kv_full(slot), T::TILE_BYTES);
-                        const CUtensorMap* map = t ? &tm_v : &tm_k;
-                        for (int blk = 0; blk < T::NBLK; ++blk) {
-                            const uint32_t dst = smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES);
-                            if (dbg_tma(dst, blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile, it.hk_idx, it.b_idx, D,
-                                        N, prm.Hk, prm.BH / prm.H, T::EB, 0x1D1))
-                                tma_load_4d(dst, map, b_kv_full(slot), blk * T::BLK_ELEMS,
-                                            (it.kv_lo + j) * kTile, it.hk_idx, it.b_idx);
-                        }
+                // The ring takes K_0, V_0, K_1, V_1, ... of the item in consecutive
+                // slots.  K_0, V_0 and K_1 complete on their own slots' barriers (they
+                // go out around the item's Q copy); from j = 1 on, V_j and K_{j+1},
+                // which the MMA warp needs at the same point (PV(j), then S(j+1)), both
+                // complete on V_j's barrier, so that it waits once per key tile.
+                // K_{j+1}'s own barrier gets a plain arrival (no bytes), so that every
+                // slot's barrier still completes one phase per use; nothing waits on it.
+                auto claim = [&](int i) -> bool {  // slot of load i is free
+                    const int round = i / T::KV_SLOTS;
+                    return round == 0 ||
+                           wait_one(b_kv_empty(i % T::KV_SLOTS), (round - 1) & 1, abort_flag, prm.st, SITE_KV_EMPTY);
+                };
+                auto copy = [&](int i, int j, bool v_tile, uint32_t bar) {  // tile of key tile j -> slot of load i
+                    const int slot = i % T::KV_SLOTS;
+                    const CUtensorMap* map = v_tile ? &tm_v : &tm_k;
+                    for (int blk = 0; blk < T::NBLK; ++blk) {
+                        const uint32_t dst = smem_u32(sKV + slot * T::TILE_BYTES + blk * T::BLK_BYTES);
+                        if (dbg_tma(dst, blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile, it.hk_idx, it.b_idx, D, N,
+                                    prm.Hk, prm.BH / prm.H, T::EB, 0x1D1))
+                            tma_load_4d(dst, map, bar, blk * T::BLK_ELEMS, (it.kv_lo + j) * kTile, it.hk_idx,
+                                        it.b_idx);
                     }
+                };
+                auto load_single = [&](int j, bool v_tile) -> bool {
+                    if (!claim(idx)) return false;
+                    const uint32_t bar = b_kv_full(idx % T::KV_SLOTS);
+                    mbar_arrive_expect_tx(bar, T::TILE_BYTES);
+                    copy(idx, j, v_tile, bar);
+                    ++idx;
+                    return true;
+                };
+                auto load_v_k = [&](int j) -> bool {  // j >= 1: V_j, and K_{j+1} if the item has it
+                    const bool k_next = j + 1 < it.n_kv;
+                    if (!claim(idx) || (k_next && !claim(idx + 1))) return false;
+                    const uint32_t bar = b_kv_full(idx % T::KV_SLOTS);
+                    mbar_arrive_expect_tx(bar, (k_next ? 2 : 1) * T::TILE_BYTES);
+                    copy(idx, j, true, bar);
+                    if (k_next) {
+                        mbar_arrive(b_kv_full((idx + 1) % T::KV_SLOTS));
+                        copy(idx + 1, j + 1, false, bar);
+                    }
+                    idx += k_next ? 2 : 1;
                     return true;
                 };
                 // The item's first key tile goes out while the previous item finishes;
                 // its Q tiles once the previous item's products that read Q are done.
-                if (it.n_kv > 0 && !load_kv(0)) {
+                if (it.n_kv > 0 && !(load_single(0, false) && load_single(0, true))) {
                     ok = false;
                     break;
                 }
@@ -269,7 +293,8 @@ __global__ void __launch_bounds__(320, 1)
                                         it.h_idx, it.b_idx);
                     }
                 }
-                for (int j = 1; j < it.n_kv && ok; ++j) ok = load_kv(j);
+                if (it.n_kv > 1) ok = load_single(1, false);
+                for (int j = 1; j < it.n_kv && ok; ++j) ok = load_v_k(j);
                 ++k;
             }
             // Let every copy this thread started land before the CTA can exit.
@@ -361,8 +386,8 @@ __global__ void __launch_bounds__(320, 1)
                         v_ready = true;
                         tc_fence_after();
                         issue_pv(0, kv_lo + j, j == 0);
-                        if (j + 1 < it.n(0)) {
-                            if (!wait_kv(kidx(kv_lo + j + 1))) return false;
+                        if (j + 1 < it.n(0)) {  // K_{j+1} landed with V_j (K_1: on its own)
+                            if (j == 0 && !wait_kv(kidx(kv_lo + 1))) return false;
                             k_next_ready = true;
                             tc_fence_after();
                             issue_s(0, kv_lo + j + 1);
@@ -378,8 +403,10 @@ __global__ void __launch_bounds__(320, 1)
                     }
                     mma_commit_warp(b_kv_empty((kidx(kv_lo + j) + 1) % T::KV_SLOTS));  // V_j consumed
                     if (j < it.n(1)) {
-                        if (j + 1 < it.n(1)) {
-                            if (!k_next_ready && !wait_kv(kidx(kv_lo + j + 1))) return false;
+                        if (j + 1 < it.n(1)) {  // K_{j+1} landed with V_j (K_1: on its own)
+                            if (!k_next_ready && !(v_ready && j > 0) &&
+                                !wait_kv(j == 0 ? kidx(kv_lo + 1) : kidx(kv_lo + j) + 1))
+                                return false;
                             tc_fence_after();
                             issue_s(1, kv_lo + j + 1);
                         } else {
@@ -405,9 +432,9 @@ __global__ void __launch_bounds__(320, 1)
                 for (int j = kv_lo; j < kv_lo + n_kv; ++j) {
                     const bool has_next = j + 1 < kv_lo + n_kv;
                     bool v_ready = false, k_next_ready = false;
-                    auto need_k_next = [&]() -> bool {
-                        if (k_next_ready) return true;
-                        if (!wait_kv(kidx(j + 1))) return false;
+                    auto need_k_next = [&]() -> bool {  // K_{j+1} lands with V_j (K_1: on its own)
+                        if (k_next_ready || (v_ready && j > kv_lo)) return true;
+                        if (!wait_kv(j == kv_lo ? kidx(kv_lo + 1) : kidx(j) + 1)) return false;
                         k_next_ready = true;
                         return true;
                     };
