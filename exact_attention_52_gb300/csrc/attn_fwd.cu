@@ -381,8 +381,11 @@ __global__ void __launch_bounds__(320, 1)
                 for (int j = 0; j < it.n_kv; ++j) {
                     bool v_ready = false, k_next_ready = false;
                     if (j < it.n(0)) {
-                        if (!wait_p(0, j)) return false;
+                        // V_j (and K_{j+1}) first: they have usually landed long before,
+                        // and checking them while P_0(j) is still being formed keeps the
+                        // check off the path from P_0(j) to PV_0(j)
                         if (!wait_kv(kidx(kv_lo + j) + 1)) return false;
+                        if (!wait_p(0, j)) return false;
                         v_ready = true;
                         tc_fence_after();
                         issue_pv(0, kv_lo + j, j == 0);
@@ -440,8 +443,8 @@ __global__ void __launch_bounds__(320, 1)
                     };
                     // query tile 0: PV_0(j), then S_0(j+1)
                     if (active(0, j)) {
+                        if (!wait_kv(kidx(j) + 1)) return false;  // before P_0(j), as above
                         if (!wait_p(0, j - it.lo(0))) return false;
-                        if (!wait_kv(kidx(j) + 1)) return false;
                         v_ready = true;
                         tc_fence_after();
                         issue_pv(0, j, j == it.lo(0));
