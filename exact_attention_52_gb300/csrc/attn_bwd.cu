@@ -2,8 +2,8 @@
 //
 //  1. bwd_pre     D_i = sum_k dO_ik O_ik (equal to sum_j P_ij dP_ij), -LSE in
 //                 log2 units, zeroed fp32 dQ accumulator.
-//  2. bwd_main    one CTA per (batch*head, 128-key tile j); loops over query
-//                 tiles i, regenerating P from Q, K and the saved log-sum-exp
+//  2. bwd_main    one work item per (key/value head, 128-key tile j); loops over
+//                 query tiles i, regenerating P from Q, K and the saved log-sum-exp
 //                 (FlashAttention item 58: backward recomputes score tiles from
 //                 inputs and normalisation statistics):
 //                     S^T  = K Q_i^T            P^T = 2^(S^T*cs - LSE*log2(e))
@@ -16,29 +16,15 @@
 //  3. dq_convert  dQ = bf16(scale * accumulator)  (the second, combining
 //                 kernel of a split reduction, CUTLASS split-K item).
 //
-// bwd_main warp roles (448 threads):
-//   warps 0-3, 4-7  compute for query half h = warp / 4 (64 queries of the
-//                   tile): P^T_h, dS^T_h, one thread per key row; dV (h = 0)
-//                   and dK (h = 1) epilogue
-//   warps 8-11      dQ writer: tensor memory -> fp32 reductions into the
-//                   accumulator (d = 128: straight from registers; d = 64:
-//                   staged in shared memory, TMA reduce-add)
-//   warp 12         TMA producer: K_j, V_j once; Q_i, dO_i, LSE2_i, D_i per step
-//   warp 13         MMA issuer
-// Tensor memory (lane = key row for S^T, dP^T, dV, dK):
-//   region h = [128 h, 128 h + 128): S^T_h at +0 (then P^T_h packed bf16),
-//              dP^T_h at +64 (once read, reused for the dQ product of half h)
-//   [256,256+D)      dV accumulator
-//   [256+D,256+2D)   dK accumulator
-// d = 128: the dQ product of half h is dQ^T_h = K^T dS^T_h (lane = feature,
-// column = query), issued right after dV/dK of half h, so that half 0's
-// reduction overlaps half 1's compute; a warp's red.global.add.f32 then covers
-// one 128-byte line of the accumulator.  d = 64: dQ_i = dS K once per step
-// (lane = query row), staged and TMA-reduced.
-// Shared memory: K, V, two stages of (Q, dO, LSE2, D), and dS^T (bf16,
-// 128-byte swizzle), read MN-major by the dQ product.  dK takes dS^T from
-// tensor memory instead (packed into the dP^T_h columns the compute warps
-// have just read), so that product reads only Q from shared memory.
+// bwd_main has two forms:
+//   d = 128  bwd_main_full_kernel: persistent CTAs, whole 128x128 query tiles,
+//            every product 128 wide, the steps pipelined so that the
+//            exponential and dS passes overlap dP^T and dV (section 2b below).
+//   d = 64   bwd_main_kernel<64>: one CTA per key tile, each query tile as two
+//            64-row halves with their own compute warpgroup and tensor-memory
+//            region, dQ staged in shared memory and TMA-reduced (section 2).
+// Both use 448 threads: warps 0-7 compute (one thread per key row), warps 8-11
+// the dQ writer, warp 12 the TMA producer, warp 13 the MMA issuer.
 #include <cuda_runtime.h>
 
 #include <type_traits>
