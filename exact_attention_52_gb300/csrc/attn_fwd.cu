@@ -404,7 +404,6 @@ __global__ void __launch_bounds__(320, 1)
                         tc_fence_after();
                         issue_pv(1, kv_lo + j, j == 0);
                     }
-                    mma_commit_warp(b_kv_empty((kidx(kv_lo + j) + 1) % T::KV_SLOTS));  // V_j consumed
                     if (j < it.n(1)) {
                         if (j + 1 < it.n(1)) {  // K_{j+1} landed with V_j (K_1: on its own)
                             if (!k_next_ready && !(v_ready && j > 0) &&
@@ -416,6 +415,9 @@ __global__ void __launch_bounds__(320, 1)
                             mma_commit_warp(b_o_full + 8u);
                         }
                     }
+                    // V_j consumed (released after S_1(j+1) is issued, which then follows
+                    // PV_1(j) without a commit in between)
+                    mma_commit_warp(b_kv_empty((kidx(kv_lo + j) + 1) % T::KV_SLOTS));
                     if (j + 2 == n_max) {  // the item's last S products have just been issued
                         mma_commit_warp(b_q_empty);
                         q_released = true;
@@ -469,7 +471,6 @@ __global__ void __launch_bounds__(320, 1)
                         issue_pv(1, j, j == it.lo(1));
                     }
                     if (!v_ready && !wait_kv(kidx(j) + 1)) return false;  // loaded, never used
-                    mma_commit_warp(b_kv_empty((kidx(j) + 1) % T::KV_SLOTS));  // V_j consumed
                     if (active(1, j)) {
                         if (active(1, j + 1)) {
                             if (!need_k_next()) return false;
@@ -483,6 +484,9 @@ __global__ void __launch_bounds__(320, 1)
                         tc_fence_after();
                         issue_s(1, j + 1);
                     }
+                    // V_j consumed (released after S_1(j+1) is issued, which then
+                    // follows PV_1(j) without a commit in between)
+                    mma_commit_warp(b_kv_empty((kidx(j) + 1) % T::KV_SLOTS));
                     if (has_next) {
                         if (!need_k_next()) return false;
                         mma_commit_warp(b_kv_empty(kidx(j + 1) % T::KV_SLOTS));  // K_{j+1} consumed
