@@ -1116,12 +1116,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     if (!wait_warp(b_p_full, g & 1, abort_flag, prm.st, SITE_P_FULL)) return false;
                     tc_fence_after();
                     issue_acc(tDK, tS + 32, stage_q(g), acc);   // dK += dS^T(t) Q_t
-                    mma_commit_warp(b_qdo_empty(g % T::STAGES));
                     // dV, dK are final after the last step's products: the epilogue may
                     // start while the last dQ product and its reductions run
                     if (t + 1 == n_steps) mma_commit_warp(b_dkv_full);
                     issue_dq();                                 // dQ^T(t), region dP
                     mma_commit_warp(b_dq_full);
+                    mma_commit_warp(b_qdo_empty(g % T::STAGES));  // Q_t, dO_t read (after dQ^T(t))
                     if (t + 1 == n_steps) mma_commit_warp(b_kv_empty);
                     if (t + 1 < n_steps) {
                         const int u = g + 1;
