@@ -175,16 +175,30 @@ long long npad(int N) { return (static_cast<long long>(N) + kTile - 1) / kTile *
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
-    size_t dq_acc, lse2, dsum, total;
+    size_t dq_acc, lse2, dsum, split_cnt, split_part, total;
+    int split_cap;  // parts of a split last round the workspace holds (0: none)
 };
 
-BwdLayout bwd_layout(int B, int H, int N, int d) {
+// fp32 dQ accumulator, -LSE log2 e, D; for d = 128 (split) also the counters and
+// partials of a split last round: at most min(kBwdSplitCap, items - 1) parts,
+// items <= B * H * ceil(N / 128) (a split needs more items than CTAs).
+BwdLayout bwd_layout(int B, int H, int N, int d, bool split) {
     const size_t rows = static_cast<size_t>(B) * H * npad(N);
     BwdLayout L;
     L.dq_acc = 0;
     L.lse2 = round256(rows * d * sizeof(float));
     L.dsum = L.lse2 + round256(rows * sizeof(float));
-    L.total = L.dsum + round256(rows * sizeof(float));
+    L.split_cnt = L.split_part = L.dsum + round256(rows * sizeof(float));
+    L.total = L.split_cnt;
+    L.split_cap = 0;
+    if (split && d == 128) {
+        const long long items = static_cast<long long>(B) * H * (npad(N) / kTile);
+        L.split_cap = static_cast<int>(items - 1 < kBwdSplitCap ? items - 1 : kBwdSplitCap);
+        if (L.split_cap > 0) {
+            L.split_part = L.split_cnt + round256(kBwdSplitCntWords * sizeof(unsigned));
+            L.total = L.split_part + round256(static_cast<size_t>(L.split_cap) * 2 * kTile * d * sizeof(float));
+        }
+    }
     return L;
 }
 
@@ -287,36 +301,46 @@ struct BwdCall {
     float* dq_acc = nullptr;
     float* lse2 = nullptr;
     float* dsum = nullptr;
+    unsigned* split_cnt = nullptr;
+    float* split_part = nullptr;
+    int split_cap = 0;
     int BH = 0, Np = 0;
 };
 
-attn_status bwd_prepare(void* workspace, int B, int H, int N, int d, float scale, int causal,
+attn_status bwd_prepare(void* workspace, int B, int H, int N, int d, float scale, int causal, bool split,
                         BwdCall* c) {
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return ATTN_ERR_INVALID;
     if ((rc = device_state(&c->ds)) != ATTN_OK) return rc;
-    const BwdLayout L = bwd_layout(B, H, N, d);
+    const BwdLayout L = bwd_layout(B, H, N, d, split);
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     c->dq_acc = reinterpret_cast<float*>(ws + L.dq_acc);
     c->lse2 = reinterpret_cast<float*>(ws + L.lse2);
     c->dsum = reinterpret_cast<float*>(ws + L.dsum);
+    c->split_cap = L.split_cap;
+    if (L.split_cap > 0) {
+        c->split_cnt = reinterpret_cast<unsigned*>(ws + L.split_cnt);
+        c->split_part = reinterpret_cast<float*>(ws + L.split_part);
+    }
     c->BH = B * H;
     c->Np = static_cast<int>(npad(N));
     return ATTN_OK;
 }
 
 attn_status bwd_pre_run(const void* o, const Strides& os, const void* dout, const Strides& dos,
-                        const float* lse, void* workspace, int B, int H, int N, int d,
+                        const float* lse, void* workspace, int B, int H, int N, int d, bool split,
                         attn_stream_t stream) {
     for (const void* p : {o, dout, static_cast<const void*>(lse)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
     if (!strides_ok(os, 2) || !strides_ok(dos, 2)) return ATTN_ERR_INVALID;
     BwdCall c;
-    attn_status rc = bwd_prepare(workspace, B, H, N, d, 1.f, 0, &c);
+    attn_status rc = bwd_prepare(workspace, B, H, N, d, 1.f, 0, split, &c);
     if (rc != ATTN_OK) return rc;
     BwdPreParams pp;
+    pp.split_cnt = c.split_cnt;
+    pp.split_cnt_words = c.split_cap > 0 ? kBwdSplitCntWords : 0;
     pp.o = o;
     pp.dout = dout;
     pp.os = os;
@@ -338,7 +362,7 @@ attn_status bwd_main_run(const void* q, const Strides& qs, const void* k, const 
                          const void* v, const Strides& vs, const void* dout, const Strides& dos,
                          void* dk, const Strides& dks, void* dv, const Strides& dvs, void* workspace,
                          int B, int H, int Hk, int N, int d, float scale, int win_left, int win_right,
-                         attn_stream_t stream) {
+                         bool split, attn_stream_t stream) {
     for (const void* p : {q, k, v, dout, static_cast<const void*>(dk), static_cast<const void*>(dv)})
         if (!aligned16(p)) return ATTN_ERR_INVALID;
     for (const Strides* st : {&qs, &ks, &vs, &dos, &dks, &dvs})
@@ -348,7 +372,7 @@ attn_status bwd_main_run(const void* q, const Strides& qs, const void* k, const 
         return rc;
     const int causal = (win_left == -1 && win_right == 0) ? 1 : 0;
     BwdCall c;
-    if ((rc = bwd_prepare(workspace, B, H, N, d, scale, causal, &c)) != ATTN_OK) return rc;
+    if ((rc = bwd_prepare(workspace, B, H, N, d, scale, causal, split, &c)) != ATTN_OK) return rc;
     CUtensorMap tq, tk, tv, tdo, tdq;
     if (!make_map(&tq, q, false, d, N, H, B, qs) || !make_map(&tk, k, false, d, N, Hk, B, ks) ||
         !make_map(&tv, v, false, d, N, Hk, B, vs) || !make_map(&tdo, dout, false, d, N, H, B, dos) ||
@@ -373,6 +397,11 @@ attn_status bwd_main_run(const void* q, const Strides& qs, const void* k, const 
     bp.win_right = win_right;
     bp.cs = scale * 1.44269504088896340736f;
     bp.scale = scale;
+    bp.split_base = bp.BHk * bp.n_kv;  // the launcher decides on a split
+    bp.split_parts = 1;
+    bp.split_cap = c.split_cap;
+    bp.split_part = c.split_part;
+    bp.split_cnt = c.split_cnt;
     bp.st = dev_status(c.ds);
     return launch_bwd_main(d, tq, tk, tv, tdo, tdq, bp, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
@@ -384,7 +413,7 @@ attn_status dq_convert_run(void* dq, const Strides& dqs, void* workspace, int B,
                            float scale, attn_stream_t stream) {
     if (!aligned16(dq) || !strides_ok(dqs, 2)) return ATTN_ERR_INVALID;
     BwdCall c;
-    attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, 0, &c);
+    attn_status rc = bwd_prepare(workspace, B, H, N, d, scale, 0, false, &c);
     if (rc != ATTN_OK) return rc;
     DqConvertParams cp;
     cp.dq_acc = c.dq_acc;
@@ -408,7 +437,7 @@ attn_status bwd_run(const void* q, const Strides& qs, const void* k, const Strid
                     const Strides& dos, const float* lse, void* dq, const Strides& dqs, void* dk,
                     const Strides& dks, void* dv, const Strides& dvs, void* workspace, int B, int H,
                     int Hk, int N, int d, float scale, int win_left, int win_right,
-                    attn_stream_t stream) {
+                    attn_stream_t stream, bool split = true) {
     const int causal = (win_left == -1 && win_right == 0) ? 1 : 0;
     attn_status rc = check_sizes(B, H, N, d, scale, causal);
     if (rc != ATTN_OK) return rc;
@@ -421,9 +450,9 @@ attn_status bwd_run(const void* q, const Strides& qs, const void* k, const Strid
         if (!strides_ok(*st, 2)) return ATTN_ERR_INVALID;
     if (workspace == nullptr || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
         return ATTN_ERR_INVALID;
-    if ((rc = bwd_pre_run(o, os, dout, dos, lse, workspace, B, H, N, d, stream)) != ATTN_OK) return rc;
+    if ((rc = bwd_pre_run(o, os, dout, dos, lse, workspace, B, H, N, d, split, stream)) != ATTN_OK) return rc;
     if ((rc = bwd_main_run(q, qs, k, ks, v, vs, dout, dos, dk, dks, dv, dvs, workspace, B, H, Hk, N, d,
-                           scale, win_left, win_right, stream)) != ATTN_OK)
+                           scale, win_left, win_right, split, stream)) != ATTN_OK)
         return rc;
     return dq_convert_run(dq, dqs, workspace, B, H, N, d, scale, stream);
 }
@@ -440,6 +469,20 @@ Strides from_abi(const attn_strides_t& s) {
 
 int check_problem(int B, int H, int N, int d, float scale, int causal) {
     return static_cast<int>(check_sizes(B, H, N, d, scale, causal));
+}
+
+size_t bwd_workspace_bytes_for(int B, int H, int N, int d, bool split) {
+    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
+    return bwd_layout(B, H, N, d, split).total;
+}
+
+int bwd_dense(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H, int N,
+              int d, float scale, int causal, bool split, cudaStream_t stream) {
+    if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
+    const Strides ds = dense(H, N, d);
+    return static_cast<int>(bwd_run(q, ds, k, ds, v, ds, o, ds, dout, ds, lse, dq, ds, dk, ds, dv, ds,
+                                    workspace, B, H, H, N, d, scale, -1, causal ? 0 : -1, stream, split));
 }
 
 cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream) {
@@ -584,15 +627,14 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
 }
 
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d) {
-    if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return 0;
-    return bwd_layout(B, H, N, d).total;
+    return bwd_workspace_bytes_for(B, H, N, d, true);
 }
 
 attn_status attn_bwd_preprocess(const void* o, const void* dout, const float* lse, void* workspace,
                                 int B, int H, int N, int d, attn_stream_t stream) {
     if (check_sizes(B, H, N, d, 1.f, 0) != ATTN_OK) return check_sizes(B, H, N, d, 1.f, 0);
     const Strides ds = dense(H, N, d);
-    return bwd_pre_run(o, ds, dout, ds, lse, workspace, B, H, N, d, stream);
+    return bwd_pre_run(o, ds, dout, ds, lse, workspace, B, H, N, d, true, stream);
 }
 
 attn_status attn_bwd_main(const void* q, const void* k, const void* v, const void* dout, void* dk,
@@ -602,7 +644,7 @@ attn_status attn_bwd_main(const void* q, const void* k, const void* v, const voi
     if (check_sizes(B, H, N, d, scale, causal) != ATTN_OK) return check_sizes(B, H, N, d, scale, causal);
     const Strides ds = dense(H, N, d);
     return bwd_main_run(q, ds, k, ds, v, ds, dout, ds, dk, ds, dv, ds, workspace, B, H, H, N, d, scale,
-                        -1, causal ? 0 : -1, stream);
+                        -1, causal ? 0 : -1, true, stream);
 }
 
 attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, int d, float scale,

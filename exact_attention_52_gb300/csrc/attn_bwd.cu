@@ -112,6 +112,8 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdPreParams
             g[k] = *reinterpret_cast<const uint4*>(dbase + n * p.dos.n);
         }
     }
+    if (blockIdx.x == 0)  // arrival counters of a split last round of the main kernel
+        for (int k = threadIdx.x; k < p.split_cnt_words; k += kAuxThreads) p.split_cnt[k] = 0u;
     // Zero this block's rows of the dQ accumulator (contiguous, fp32 [BH, Npad, D]).
     float4* z = reinterpret_cast<float4*>(p.dq_acc + (static_cast<size_t>(bh) * p.Npad + n0) * D);
 #pragma unroll
@@ -175,12 +177,15 @@ struct BwdWork {
     int q_bh0;           // first query (batch, head) index of the group
     int b_idx, hk_idx;   // batch, key/value head
     int bH0;             // (batch, head) index of head 0 of this batch
-    int n_steps;         // G * n_qh
+    int n_steps;         // G * n_qh (a part of a split item: its share of them)
+    int slot;            // a part of a split item: its index among the split round's parts; else -1
+    int parts;           // parts of the item (1: whole)
+    int tt0, bh_first;   // (tile step, query head) of the first step
 
     __device__ explicit BwdWork(const BwdParams& prm) : BwdWork(prm, static_cast<int>(blockIdx.x)) {}
 
     // Work item `item` of the launch's numbering (items = key tiles of every
-    // key/value head).
+    // key/value head), whole.
     __device__ BwdWork(const BwdParams& prm, int item) {
         const int N = prm.N;
         // Non-causal: head-major order keeps the resident CTAs on a few heads, so
@@ -206,6 +211,26 @@ struct BwdWork {
         hk_idx = kv_bh % prm.Hk;
         bH0 = b_idx * prm.H;
         n_steps = G * n_qh;
+        slot = -1;
+        parts = 1;
+        tt0 = 0;
+        bh_first = q_bh0;
+    }
+    // Item `v` of a launch with a split last round: from split_base on, part
+    // (v - split_base) % P of item split_base + (v - split_base) / P, which takes
+    // steps [t0, t1) of the item's walk (query head by query head, tile by tile).
+    __device__ static BwdWork split_at(const BwdParams& prm, int v) {
+        if (v < prm.split_base) return BwdWork(prm, v);
+        const int s = v - prm.split_base, P = prm.split_parts;
+        BwdWork w(prm, prm.split_base + s / P);
+        const int part = s % P;
+        const int t0 = part * w.n_steps / P;
+        w.n_steps = (part + 1) * w.n_steps / P - t0;
+        w.slot = s;
+        w.parts = P;
+        w.tt0 = t0 % w.n_qh;
+        w.bh_first = w.q_bh0 + t0 / w.n_qh;
+        return w;
     }
     // Query tile of step t (tt = step index within one query head).  Over the
     // full range each key tile starts at its own index and wraps, so CTAs that
@@ -761,6 +786,67 @@ struct BwdFullTraits {
 
 enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C, SITE_AUG_FULL = 0x20D, SITE_PA_FULL = 0x20E };
 
+// Epilogue of one warp's 32 rows (row r of this lane) of dV (h = 0) or dK (h = 1,
+// written times f = scale) for a part of a split item: the part's fp32 partial
+// rows (tensor memory at tsrc) go to its slot of the workspace; the item's last
+// part to arrive for these rows adds up every part's partial in part order (so
+// the result does not depend on which part is last), writes the bf16 rows and
+// leaves the counter at zero.  Kept out of line so that the main loops'
+// registers do not depend on it.
+__device__ __noinline__ void split_part_epilogue(float* split_part, unsigned* split_cnt, int slot, int parts,
+                                                 int h, int wq, int r, uint32_t tsrc, uint8_t* dst,
+                                                 bool row_ok, float f) {
+    constexpr int D = 128;
+    const int lane = threadIdx.x & 31;
+    const int item_slot = slot / parts;
+    auto part_row = [&](int sub) { return split_part + ((static_cast<size_t>(sub) * 2 + h) * kTile + r) * D; };
+    float* mine = part_row(slot);
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(tsrc + 32 * c, o);
+        tmem_ld_wait(o);
+#pragma unroll
+        for (int v = 0; v < 8; ++v)
+            st_global_v4(mine + c * 32 + 4 * v, o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+    }
+    __threadfence();
+    __syncwarp();
+    unsigned* cnt = split_cnt + (item_slot * 2 + h) * 4 + wq;
+    unsigned arrived = 0;
+    if (lane == 0) arrived = atomicAdd(cnt, 1u);
+    arrived = __shfl_sync(0xffffffffu, arrived, 0);
+    if (arrived != static_cast<unsigned>(parts - 1)) return;
+    if (lane == 0) *cnt = 0u;  // every part has arrived
+    __threadfence();
+#pragma unroll 1
+    for (int c = 0; c < D / 32; ++c) {
+        float a[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) a[e] = 0.f;
+#pragma unroll 1
+        for (int q = 0; q < parts; ++q) {
+            const float4* src = reinterpret_cast<const float4*>(part_row(item_slot * parts + q) + c * 32);
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+                const float4 x = __ldcg(src + v);
+                a[4 * v] += x.x;
+                a[4 * v + 1] += x.y;
+                a[4 * v + 2] += x.z;
+                a[4 * v + 3] += x.w;
+            }
+        }
+        if (row_ok) {
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                st_global_v4(dst + c * 64 + v * 16, pack_bf16x2(a[8 * v] * f, a[8 * v + 1] * f),
+                             pack_bf16x2(a[8 * v + 2] * f, a[8 * v + 3] * f),
+                             pack_bf16x2(a[8 * v + 4] * f, a[8 * v + 5] * f),
+                             pack_bf16x2(a[8 * v + 6] * f, a[8 * v + 7] * f));
+        }
+    }
+}
+
 // v as hi + mid + lo, each rounded to bf16 (hi + mid + lo = v to about 2^-24
 // relative: each remainder is exact in fp32), returned halved (exact) and
 // packed as the bf16 words (hi/2 | mid/2 << 16, lo/2).
@@ -777,6 +863,7 @@ __device__ __forceinline__ uint2 split3_half_bf16(float v) {
 // Pause of the dQ writer between groups of eight reductions (see the writer).
 constexpr unsigned kDqPauseNs = 60;
 
+template <bool SPLIT>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -820,7 +907,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // epilogue (dV, dK out of tensor memory) overlaps the next item's K/V copy
     // and first products.  item_at returns -1 after the last round and -2 for a
     // round in which this CTA has no item (only the last round can be short).
-    const int n_items = prm.BHk * prm.n_kv;
+    const int n_items =
+        SPLIT ? prm.split_base + (prm.BHk * prm.n_kv - prm.split_base) * prm.split_parts : prm.BHk * prm.n_kv;
+    auto work = [&](int v) {  // the work of item v (a part of a split item from split_base on)
+        if constexpr (SPLIT) return BwdWork::split_at(prm, v);
+        else return BwdWork(prm, v);
+    };
     auto item_at = [&](int r) -> int {
         const long long base = static_cast<long long>(r) * gridDim.x;
         if (base >= n_items) return -1;
@@ -908,10 +1000,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int item = item_at(rr);
                 if (item == -1) return;
                 if (item < 0) continue;
-                const BwdWork w(prm, item);
+                const BwdWork w = work(item);
                 if (w.n_steps > 0) {
-                    bh = w.q_bh0;
-                    tile = w.q_tile(0);
+                    bh = w.bh_first;
+                    tile = w.q_tile(w.tt0);
                     return;
                 }
             }
@@ -977,10 +1069,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int item = item_at(r);
             if (item == -1) break;
             if (item < 0) continue;
-            const BwdWork w(prm, item);
+            const BwdWork w = work(item);
             int nx_bh, nx_tile;  // first step of the next item with steps
             first_step(r + 1, nx_bh, nx_tile);
-            int tt = 0, bh = w.q_bh0;
+            int tt = w.tt0, bh = w.bh_first;
             // (query head, tile) of the step after step t of this item
             auto after = [&](int t, int& nbh, int& ni) {
                 if (t + 1 >= w.n_steps) {
@@ -996,7 +1088,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // the item's first Q/dO stage goes out as soon as a stage is free,
             // then K and V once the previous item's last products have read them
             after(0, nbh, ni);
-            if (w.n_steps > 0 && !load_step(w.q_tile(0), bh, w.bH0, w.b_idx, nbh, ni)) {
+            if (w.n_steps > 0 && !load_step(w.q_tile(tt), bh, w.bH0, w.b_idx, nbh, ni)) {
                 ok = false;
                 break;
             }
@@ -1144,7 +1236,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int item = item_at(r);
                 if (item == -1) break;
                 if (item < 0) continue;
-                const BwdWork w(prm, item);
+                const BwdWork w = work(item);
                 if (w.n_steps == 0) {  // nothing sees this key tile: zero dV, dK, release K/V
                     if (!wait_warp(b_kv, k & 1, abort_flag, prm.st, SITE_KV)) break;
                     mma_commit_warp(b_dkv_full);
@@ -1176,9 +1268,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const int item = item_at(rr);
         if (item == -1) break;
         if (item < 0) continue;
-        const BwdWork w(prm, item);
+        const BwdWork w = work(item);
         const int kv_row = w.j * kTile + r;
-        for (int t = 0, tt = 0; t < w.n_steps; ++t, ++tt, ++g) {
+        for (int t = 0, tt = w.tt0; t < w.n_steps; ++t, ++tt, ++g) {
             if (tt == w.n_qh) tt = 0;
             const int i = w.q_tile(tt);
             if (!wait_warp(b_s_full, g & 1, abort_flag, prm.st, SITE_S_FULL)) {
@@ -1279,13 +1371,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             break;
         }
         tc_fence_after();
-        {
-            const bool row_ok = kv_row < N;
-            const Strides& ds = h ? prm.dks : prm.dvs;
-            const long long roff = (w.b_idx * ds.b + w.hk_idx * ds.h + (row_ok ? kv_row : 0) * ds.n) * 2;
-            const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
-            uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
-            const float f = h ? prm.scale : 1.f;
+        const bool row_ok = kv_row < N;
+        const Strides& ds = h ? prm.dks : prm.dvs;
+        const long long roff = (w.b_idx * ds.b + w.hk_idx * ds.h + (row_ok ? kv_row : 0) * ds.n) * 2;
+        const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
+        uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
+        const float f = h ? prm.scale : 1.f;
+        if (SPLIT && w.slot >= 0) {
+            split_part_epilogue(prm.split_part, prm.split_cnt, w.slot, w.parts, h, wq, r, tsrc, dst, row_ok, f);
+        } else {
             const bool empty = w.n_steps == 0;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
@@ -1322,9 +1416,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int item = item_at(rr);
             if (item == -1) break;
             if (item < 0) continue;
-            const BwdWork w(prm, item);
+            const BwdWork w = work(item);
             const bool last_item = item_at(rr + 1) < 0;
-            int tt = 0, bh = w.q_bh0;
+            int tt = w.tt0, bh = w.bh_first;
             for (int t = 0; t < w.n_steps; ++t, ++tt, ++g) {
                 if (tt == w.n_qh) {
                     tt = 0;
@@ -1423,20 +1517,44 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
     if (D == 128) {
         using T = BwdFullTraits;
         static const cudaError_t attr = cudaFuncSetAttribute(
-            bwd_main_full_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+            bwd_main_full_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
         if (attr != cudaSuccess) return attr;
+        static const cudaError_t attr_split = cudaFuncSetAttribute(
+            bwd_main_full_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+        if (attr_split != cudaSuccess) return attr_split;
         // persistent: one CTA per SM (shared memory admits one), items in snake order
-        long long grid = static_cast<long long>(p.BHk) * p.n_kv;
+        const long long items = static_cast<long long>(p.BHk) * p.n_kv;
+        long long grid = items;
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
         if (sms < grid) grid = sms;
         if (grid < 1) return cudaSuccess;
+        // Split the last round when it would leave CTAs idle (no mask: every item
+        // has the same steps), into P = grid / r parts per item, P >= 2.
+        BwdParams pp = p;
+        pp.split_base = static_cast<int>(items);
+        pp.split_parts = 1;
+        const long long rem = items % grid;
+        const long long steps = static_cast<long long>(p.H / p.Hk) * p.n_kv;
+        if (rem > 0 && p.causal == 0 && p.win_left < 0 && p.win_right < 0 && p.split_cap > 0) {
+            long long parts = grid / rem;
+            if (parts > steps) parts = steps;
+            if (parts * rem > p.split_cap) parts = p.split_cap / rem;
+            if (parts >= 2) {
+                pp.split_base = static_cast<int>(items - rem);
+                pp.split_parts = static_cast<int>(parts);
+            }
+        }
         const cudaError_t dbg = dbg_set_word(p.st.word, stream);
         if (dbg != cudaSuccess) return dbg;
-        bwd_main_full_kernel<<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
-            tq, tk, tv, tdo, p);
+        if (pp.split_parts > 1)
+            bwd_main_full_kernel<true><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
+                tq, tk, tv, tdo, pp);
+        else
+            bwd_main_full_kernel<false><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
+                tq, tk, tv, tdo, pp);
         return cudaGetLastError();
     }
     return cudaErrorInvalidValue;

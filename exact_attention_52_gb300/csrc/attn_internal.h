@@ -57,8 +57,20 @@ struct BwdPreParams {
     float* dq_acc;     // fp32 [BH, Npad, D], zeroed here
     float* lse2;       // fp32 [BH, Npad]: -LSE * log2(e); -inf on padding rows
     float* dsum;       // fp32 [BH, Npad]: D_i = sum_k dO_ik O_ik; 0 on padding rows
+    unsigned* split_cnt;  // arrival counters of split key tiles (see BwdParams), zeroed here
+    int split_cnt_words;  // 0: none
     int N, Npad, BH, H, D;
 };
+
+// Split last round of the d = 128 backward (no mask only).  With G CTAs and
+// n = R G + r items (key tiles), r > 0, the last round would leave G - r CTAs
+// idle for a whole item.  Instead each of its r items is dealt as P = G / r
+// parts (contiguous ranges of its query steps, P >= 2); every part leaves its
+// fp32 dV and (unscaled) dK partial in the workspace, and the last part of an
+// item to finish (counted per 32-row warp slice) adds the others' partials to
+// its own and writes the item's dV and dK.  At most kBwdSplitCap parts.
+constexpr int kBwdSplitCap = 160;
+constexpr int kBwdSplitCntWords = kBwdSplitCap * 8;  // [item slot][dV, dK][4 warp slices]
 
 struct BwdParams {
     const float* lse2;  // workspace (-LSE * log2(e)), see BwdPreParams
@@ -76,6 +88,14 @@ struct BwdParams {
     int win_right;
     float cs;           // scale * log2(e)
     float scale;        // softmax scale (applied to dK here and to dQ at conversion)
+    // Split last round (d = 128): virtual items v >= split_base are part v - split_base
+    // of P = split_parts parts of item split_base + (v - split_base) / P.  Without a
+    // split: split_base = number of items, split_parts = 1.
+    int split_base;
+    int split_parts;
+    int split_cap;        // parts the workspace has room for (0: no split possible)
+    float* split_part;    // fp32 [part][dV, dK][128 rows][D]
+    unsigned* split_cnt;  // kBwdSplitCntWords counters, zero at launch
     DevStatus st;
 };
 
@@ -103,6 +123,14 @@ cudaError_t launch_wait_selftest(DevStatus st, cudaStream_t stream);
 // Problem check shared by the entry points (sizes, head dim, scale, causal
 // flag); returns an attn_status value (0 = valid).
 int check_problem(int B, int H, int N, int d, float scale, int causal);
+
+// The dense backward with or without the split last round of the d = 128
+// kernel (without it the workspace has no room for its partials): the workspace
+// size it needs, and the call (an attn_status value).
+size_t bwd_workspace_bytes_for(int B, int H, int N, int d, bool split);
+int bwd_dense(const void* q, const void* k, const void* v, const void* o, const void* dout,
+              const float* lse, void* dq, void* dk, void* dv, void* workspace, int B, int H, int N,
+              int d, float scale, int causal, bool split, cudaStream_t stream);
 
 // Shared-memory bytes a launcher requests (for tests of the host logic).
 int fwd_smem_bytes(int D, bool fp8);

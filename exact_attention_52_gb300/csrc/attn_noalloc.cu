@@ -78,11 +78,21 @@ extern "C" attn_status attn_bwd_noalloc(const void* q, const void* k, const void
     if (causal != 0 && causal != 1) return ATTN_ERR_INVALID;
     const attn_status chk = static_cast<attn_status>(attn::check_problem(B, H, N, d, scale, causal));
     if (chk != ATTN_OK) return chk;
-    const size_t need = attn_bwd_workspace_bytes(B, H, N, d);
+    // With the split last round of the d = 128 kernel when its partials fit in the
+    // scratch too (the results are then attn_bwd's bit for bit); otherwise without
+    // it, and rows of the last round's key tiles of dK, dV may differ from
+    // attn_bwd's in the last bit (another summation order).
+    bool split = true;
+    size_t need = attn::bwd_workspace_bytes_for(B, H, N, d, true);
+    if (need > kNoAllocScratchBytes) {
+        split = false;
+        need = attn::bwd_workspace_bytes_for(B, H, N, d, false);
+    }
     if (need == 0) return ATTN_ERR_INVALID;
     if (need > kNoAllocScratchBytes) return ATTN_ERR_UNSUPPORTED;
     void* scratch = nullptr;
     const attn_status rc = scratch_for_current_device(&scratch);
     if (rc != ATTN_OK) return rc;
-    return attn_bwd(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, H, N, d, scale, causal, stream);
+    return static_cast<attn_status>(
+        attn::bwd_dense(q, k, v, o, dout, lse, dq, dk, dv, scratch, B, H, N, d, scale, causal, split, stream));
 }

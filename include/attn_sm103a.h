@@ -79,7 +79,10 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
 /*
  * Bytes of device scratch attn_bwd needs for (B, H, N, d): an fp32 dQ
  * accumulator [B*H, Npad, d] plus two fp32 vectors [B*H, Npad] (LSE in log2
- * units and D), Npad = N rounded up to 128.  Returns 0 for invalid sizes.
+ * units and D), Npad = N rounded up to 128; for d = 128 also 5 KB of counters
+ * and room for fp32 dV/dK partials of min(160, B*H*Npad/128 - 1) parts of a
+ * split last round of key tiles (128 KB each; see attn_bwd).  Every region
+ * starts on a 256-byte boundary.  Returns 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -94,7 +97,11 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  * accumulator), main (recompute P, accumulate dV, dK in tensor memory, add
  * dQ partial tiles into the accumulator with fp32 reductions), and dQ
  * conversion.  dQ's summation order varies from run to run (scatter-add
- * item 52); dK and dV are deterministic.
+ * item 52); dK and dV are deterministic.  d = 128 without a mask: the main
+ * kernel's CTAs (one per SM) take key tiles in rounds; when the last round
+ * has fewer key tiles than CTAs, each of them is shared by several CTAs (its
+ * query tiles split into parts), whose fp32 dV/dK partials are added in the
+ * workspace in part order by the last part to finish.
  * Source: ai.engineer item 58 (backward regenerates score tiles from saved
  * normalisation statistics); FlashAttention-3 digest section 1 (dQ-writer
  * warp and atomic accumulation); the gradient formulas are the calculus of
@@ -135,10 +142,15 @@ attn_status attn_bwd_dq_convert(void* dq, void* workspace, int B, int H, int N, 
  *   The problem is checked first, as attn_bwd checks it, with the same
  *   status (ATTN_ERR_INVALID for bad sizes, scale or flag,
  *   ATTN_ERR_UNSUPPORTED for a head dim other than 64 or 128); a valid
- *   problem whose attn_bwd_workspace_bytes() exceeds 64 MiB is then rejected
- *   with ATTN_ERR_UNSUPPORTED, before anything is launched (about 129k padded
- *   rows at d = 128, e.g. B*H*ceil(N/128)*128 <= 129,000).  Pointer and
- *   launch errors are those of attn_bwd.
+ *   problem is then rejected with ATTN_ERR_UNSUPPORTED, before anything is
+ *   launched, when even the scratch without the split last round's partials
+ *   exceeds 64 MiB (about 129k padded rows at d = 128, e.g.
+ *   B*H*ceil(N/128)*128 <= 129,000).  Where attn_bwd_workspace_bytes() fits
+ *   the 64 MiB the results are attn_bwd's bit for bit; between the two sizes
+ *   the d = 128 main kernel runs without the split last round, and dK, dV
+ *   rows of its last round's key tiles may differ from attn_bwd's in the last
+ *   bit (another summation order).  Pointer and launch errors are those of
+ *   attn_bwd.
  *   Every call looks up the array's device address in the current context
  *   (a lookup, no allocation), so the entry point stays valid after
  *   cudaDeviceReset or a change of context.  The first call in a context may

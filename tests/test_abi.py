@@ -46,12 +46,17 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # fp32 dQ accumulator over padded rows + two fp32 vectors, 256-byte rounded
-    B, H, N, d = 2, 3, 200, 128
-    npad = 256
-    rows = B * H * npad
+    # fp32 dQ accumulator over padded rows + two fp32 vectors, 256-byte rounded;
+    # d = 128 adds the counters (160 x 8 words) and fp32 dV/dK partials of a split
+    # last round: min(160, items - 1) parts of 2 x 128 x d floats, items = B*H*ceil(N/128)
     r256 = lambda x: (x + 255) // 256 * 256
-    assert lib.attn_bwd_workspace_bytes(B, H, N, d) == r256(rows * d * 4) + 2 * r256(rows * 4)
+    for B, H, N, d in ((2, 3, 200, 128), (2, 3, 200, 64), (1, 1, 128, 128), (1, 32, 8192, 128)):
+        npad = (N + 127) // 128 * 128
+        rows = B * H * npad
+        base = r256(rows * d * 4) + 2 * r256(rows * 4)
+        cap = min(160, B * H * npad // 128 - 1) if d == 128 else 0
+        split = r256(160 * 8 * 4) + r256(cap * 2 * 128 * d * 4) if cap > 0 else 0
+        assert lib.attn_bwd_workspace_bytes(B, H, N, d) == base + split, (B, H, N, d)
     assert lib.attn_bwd_workspace_bytes(0, 1, 1, 64) == 0
     assert lib.attn_bwd_workspace_bytes(1, 1, 1, 96) == 0
 
@@ -120,5 +125,8 @@ def test_noalloc_checks_the_problem_before_its_scratch_limit(lib):
     assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 128, 0.1, 2, None) == INVALID
     assert lib.attn_bwd_noalloc(*args, 1, 1, 128, 128, float("inf"), 0, None) == INVALID
     assert lib.attn_bwd_noalloc(*args, 1, 32, 8192, 128, 0.088, 0, None) == UNSUP
-    assert lib.attn_bwd_workspace_bytes(1, 15, 8192, 128) <= 64 << 20 < lib.attn_bwd_workspace_bytes(
-        1, 32, 8192, 128)
+    # without the split last round's partials (which it leaves out when they do
+    # not fit) B1 H15 N8192 d128 fits the scratch and B1 H32 N8192 does not
+    r256 = lambda x: (x + 255) // 256 * 256
+    unsplit = lambda H: r256(H * 8192 * 128 * 4) + 2 * r256(H * 8192 * 4)
+    assert unsplit(15) <= 64 << 20 < unsplit(32)

@@ -3,12 +3,16 @@ memory (code handed only its input and output tensors by a framework that owns
 all device memory).  It runs on a fixed scratch array inside the library.
 
 Checked through the C ABI against attn_bwd (which takes a caller-allocated
-workspace) on three calls in a row with different inputs and sizes -- a small
-one, one that uses nearly all of the 64 MiB scratch, then a small one again --
+workspace) on four calls in a row with different inputs and sizes -- a small
+one, two that use nearly all of the 64 MiB scratch, then a small one again --
 so that anything left in the shared scratch by an earlier call would show up
 in a later one:
   * dK and dV come from the same deterministic kernels and must be
-    bit-identical to attn_bwd's;
+    bit-identical to attn_bwd's where the workspace layout of attn_bwd fits in
+    the scratch (B1 H10 N8192, whose last round of key tiles is split into
+    parts); where it does not (B1 H15 N8192) the call runs without the split
+    last round, and the rows of those key tiles are summed in another order:
+    compared within the rounding of their bf16 output;
   * dQ is summed by fp32 reductions in an order that may differ between the
     two calls, so it is compared within the rounding of its bf16 output;
   * all three gradients are also compared with the fp64 oracle.
@@ -44,15 +48,18 @@ def _call_noalloc(lib, q, k, v, o, do, lse, causal):
     return dq, dk, dv
 
 
-# (B, H, N, d, oracle heads): the middle call needs 61 MiB of scratch
-CALLS = [(1, 3, 700, 128, None), (1, 15, 8192, 128, [(0, 7)]), (2, 2, 513, 64, None)]
+# (B, H, N, d, oracle heads): the middle calls need 60 MiB (with the split last
+# round's partials) and 61 MiB (without them) of scratch
+CALLS = [(1, 3, 700, 128, None), (1, 10, 8192, 128, [(0, 9)]), (1, 15, 8192, 128, [(0, 7)]),
+         (2, 2, 513, 64, None)]
 
 
 @pytest.mark.parametrize("causal", [False, True])
 def test_noalloc_matches_workspace_backward_three_calls(causal):
     lib = api.load_library()
     for call, (B, H, N, d, heads) in enumerate(CALLS):
-        assert lib.attn_bwd_workspace_bytes(B, H, N, d) <= SCRATCH_BYTES
+        same_layout = lib.attn_bwd_workspace_bytes(B, H, N, d) <= SCRATCH_BYTES
+        assert same_layout or (B, H, N, d) == (1, 15, 8192, 128)
         inp = make_inputs(B, H, N, d, seed=40 + call + 10 * int(causal), with_grad=True)
         q, k, v, do = (bf16_to_device(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
         o, lse = api.fwd(q, k, v, causal=causal)
@@ -62,8 +69,12 @@ def test_noalloc_matches_workspace_backward_three_calls(causal):
         assert rc == 0, f"device error {rc} at site {site:#x}"
         dq_g, dk_g, dv_g = (device_bf16_to_f64(t) for t in got)
         dq_r, dk_r, dv_r = (device_bf16_to_f64(t) for t in ref)
-        assert np.array_equal(dk_g, dk_r), (call, "dk")
-        assert np.array_equal(dv_g, dv_r), (call, "dv")
+        if same_layout:
+            assert np.array_equal(dk_g, dk_r), (call, "dk")
+            assert np.array_equal(dv_g, dv_r), (call, "dv")
+        else:
+            assert rel_fro(dk_g, dk_r) <= 1e-3, (call, "dk", rel_fro(dk_g, dk_r))
+            assert rel_fro(dv_g, dv_r) <= 1e-3, (call, "dv", rel_fro(dv_g, dv_r))
         assert rel_fro(dq_g, dq_r) <= 1e-4, (call, rel_fro(dq_g, dq_r))
         qd, kd, vd, dod = decoded(inp)
         scale = 1.0 / np.sqrt(d)
