@@ -96,3 +96,18 @@ def test_debug_build_splitkv_and_fp8():
     assert bf16_out_err(device_bf16_to_f64(o), o_ref) <= TOL_O_MAXABS
     o8_ref, _ = oracle.forward(*decoded_fp8(f8), 1.0 / np.sqrt(128), True)
     assert rel_fro(device_bf16_to_f64(o8), o8_ref) <= TOL_FP8_RELFRO
+
+
+def test_debug_build_split_last_round():
+    """d = 128 without a mask, 160 key-tile items for 152 CTAs: the last round's
+    8 items are split into 19 parts each, whose partials meet in the workspace."""
+    inp = make_inputs_gqa(1, 20, 10, 2048, 128, seed=91, with_grad=True)
+    with debug_library():
+        q, k, v, do = (bf16_to_device(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+        o, lse = api.fwd(q, k, v, causal=False)
+        dq, dk, dv = api.bwd(q, k, v, o, do, lse, causal=False)
+        _assert_clean()
+    qf, kf, vf, dof = decoded(inp)
+    refs = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), False)
+    for g, r in zip((dq, dk, dv), refs):
+        assert grad_rel_err(device_bf16_to_f64(g), r) <= TOL_GRAD_RELFRO
