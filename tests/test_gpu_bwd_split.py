@@ -61,3 +61,25 @@ def test_split_last_round_is_deterministic():
     second = api.bwd(*args, causal=False)
     for name, a, b in zip(("dk", "dv"), first[1:], second[1:]):
         assert np.array_equal(device_bf16_to_f64(a), device_bf16_to_f64(b)), name
+
+
+def test_split_last_round_bnhd_layout():
+    """A split last round writing dK and dV through [B, N, H, d] strides (rows of
+    a key tile 8 heads apart) with grouped heads: 2 x 4 kv heads x 20 key tiles
+    = 160 items, the last 8 in 19 parts."""
+    B, H, Hk, N = 2, 8, 4, 2560
+    inp = make_inputs_gqa(B, H, Hk, N, 128, seed=606, with_grad=True)
+
+    def to_bnhd(t):
+        return t.permute(0, 2, 1, 3).contiguous()
+
+    q, k, v, do = (to_bnhd(bf16_to_device(x)) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+    o, lse = api.fwd_strided(q, k, v, layout="bnhd", window=(-1, -1))
+    grads = api.bwd_strided(q, k, v, o, do, lse, layout="bnhd", window=(-1, -1))
+    rc, site = api.check_device_error()
+    assert rc == 0, f"device error {rc} at site {site:#x}"
+    qf, kf, vf, dof = decoded(inp)
+    ref = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), False)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        err = grad_rel_err(device_bf16_to_f64(g.permute(0, 2, 1, 3)), r)
+        assert err <= TOL_GRAD_RELFRO, (name, err)
