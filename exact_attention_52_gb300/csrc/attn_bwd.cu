@@ -29,7 +29,12 @@
 // the dQ writer, warp 12 the TMA producer, warp 13 the MMA issuer.
 #include <cuda_runtime.h>
 
+#include <algorithm>
+#include <mutex>
+#include <queue>
 #include <type_traits>
+#include <utility>
+#include <vector>
 
 #include "attn_internal.h"
 #include "ptx.cuh"
@@ -225,14 +230,24 @@ struct BwdWork {
         if (v < prm.split_base) return BwdWork(prm, v);
         const int s = v - prm.split_base, P = prm.split_parts;
         BwdWork w(prm, prm.split_base + s / P);
-        const int part = s % P;
-        const int t0 = part * w.n_steps / P;
-        w.n_steps = (part + 1) * w.n_steps / P - t0;
-        w.slot = s;
-        w.parts = P;
-        w.tt0 = t0 % w.n_qh;
-        w.bh_first = w.q_bh0 + t0 / w.n_qh;
+        w.make_part(s % P, P, s);
         return w;
+    }
+    // Entry e of a dealt launch (see BwdDeal): item e & 0x3FFF, whole, or (bit 15)
+    // part (e >> 14) & 1 of its two parts, with partial slot 2 * item + part.
+    __device__ static BwdWork dealt(const BwdParams& prm, int e) {
+        const int item = e & 0x3FFF;
+        BwdWork w(prm, item);
+        if (e & 0x8000) w.make_part((e >> 14) & 1, 2, 2 * item + ((e >> 14) & 1));
+        return w;
+    }
+    __device__ void make_part(int part, int P, int part_slot) {
+        const int t0 = part * n_steps / P;
+        n_steps = (part + 1) * n_steps / P - t0;
+        slot = part_slot;
+        parts = P;
+        tt0 = t0 % n_qh;
+        bh_first = q_bh0 + t0 / n_qh;
     }
     // Query tile of step t (tt = step index within one query head).  Over the
     // full range each key tile starts at its own index and wraps, so CTAs that
@@ -788,6 +803,23 @@ struct BwdFullTraits {
 
 enum : uint32_t { SITE_DP_FULL = 0x20B, SITE_KV_EMPTY = 0x20C, SITE_AUG_FULL = 0x20D, SITE_PA_FULL = 0x20E };
 
+// Per-CTA item lists of a dealt launch (bwd_main_full_kernel<2>), for causal
+// launches whose longest items (a key tile visits every query head of its group,
+// so causal items run from G n_q steps down to G) reach or pass the per-CTA mean:
+// the longest are split in two parts (steps [0, n/2) and [n/2, n) of the item's
+// walk, partial slots 2 item + part) and the parts and whole items are dealt
+// longest first, each to the CTA with the least work so far.  The lists are
+// built on the host and travel as a kernel parameter.
+constexpr int kDealGrid = 160;   // CTAs the lists cover at most
+constexpr int kDealMax = 2048;   // entries (items and parts) at most
+template <int MODE>
+struct BwdDealArg {};
+template <>
+struct BwdDealArg<2> {
+    uint16_t start[kDealGrid + 1];  // CTA c takes entries [start[c], start[c + 1])
+    uint16_t entry[kDealMax];       // item | part << 14 | (split ? 1 << 15 : 0)
+};
+
 // Epilogue of one warp's 32 rows (row r of this lane) of dV (h = 0) or dK (h = 1,
 // written times f = scale) for a part of a split item: the part's fp32 partial
 // rows (tensor memory at tsrc) go to its slot of the workspace; the item's last
@@ -865,11 +897,13 @@ __device__ __forceinline__ uint2 split3_half_bf16(float v) {
 // Pause of the dQ writer between groups of eight reductions (see the writer).
 constexpr unsigned kDqPauseNs = 60;
 
-template <bool SPLIT>
+// MODE 0: items dealt in snake order; 1: the same with a split last round; 2: the
+// per-CTA lists of a BwdDeal (causal launches with long items).
+template <int MODE>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
-                         const BwdParams prm) {
+                         const BwdParams prm, const __grid_constant__ BwdDealArg<MODE> deal) {
     using T = BwdFullTraits;
     constexpr int D = T::D;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -909,13 +943,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     // epilogue (dV, dK out of tensor memory) overlaps the next item's K/V copy
     // and first products.  item_at returns -1 after the last round and -2 for a
     // round in which this CTA has no item (only the last round can be short).
-    const int n_items =
-        SPLIT ? prm.split_base + (prm.BHk * prm.n_kv - prm.split_base) * prm.split_parts : prm.BHk * prm.n_kv;
+    const int n_items = MODE == 1 ? prm.split_base + (prm.BHk * prm.n_kv - prm.split_base) * prm.split_parts
+                                  : prm.BHk * prm.n_kv;
     auto work = [&](int v) {  // the work of item v (a part of a split item from split_base on)
-        if constexpr (SPLIT) return BwdWork::split_at(prm, v);
+        if constexpr (MODE == 1) return BwdWork::split_at(prm, v);
+        else if constexpr (MODE == 2) return BwdWork::dealt(prm, v);
         else return BwdWork(prm, v);
     };
     auto item_at = [&](int r) -> int {
+        if constexpr (MODE == 2) {  // entry r of this CTA's list
+            const int e = deal.start[blockIdx.x] + r;
+            return e < deal.start[blockIdx.x + 1] ? static_cast<int>(deal.entry[e]) : -1;
+        }
         const long long base = static_cast<long long>(r) * gridDim.x;
         if (base >= n_items) return -1;
         const int c = (r & 1) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
@@ -1379,7 +1418,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const uint32_t tsrc = tmem + (h ? T::COL_DK : T::COL_DV) + lane_off;
         uint8_t* dst = static_cast<uint8_t*>(h ? prm.dk : prm.dv) + roff;
         const float f = h ? prm.scale : 1.f;
-        if (SPLIT && w.slot >= 0) {
+        if (MODE != 0 && w.slot >= 0) {
             split_part_epilogue(prm.split_part, prm.split_cnt, w.slot, w.parts, h, wq, r, tsrc, dst, row_ok, f);
         } else {
             const bool empty = w.n_steps == 0;
@@ -1474,6 +1513,120 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     }
 }
 
+// Host side of BwdDealArg<2>: the predicted end of the launch (in steps, an
+// item costing its steps plus kDealItemCost) of the snake order against the
+// deal with the longest items split, for a few split thresholds; the best deal
+// is used when it ends at least 3 % sooner.  Results are cached per shape.
+constexpr double kDealItemCost = 1.5;  // per-item overhead in steps (clock stamps: ~3.4 us / 2.3 us)
+
+double snake_makespan(const std::vector<double>& cost, int grid) {
+    std::vector<double> load(grid, 0.0);
+    const int n = static_cast<int>(cost.size());
+    for (int r = 0; static_cast<long long>(r) * grid < n; ++r)
+        for (int c = 0; c < grid; ++c) {
+            const long long i = static_cast<long long>(r) * grid + ((r & 1) ? grid - 1 - c : c);
+            if (i < n) load[c] += cost[i];
+        }
+    return *std::max_element(load.begin(), load.end());
+}
+
+// Deal of the n causal items of p (item i: key tile i / BHk, longest first) with
+// the x longest split in two, longest entry first onto the least-loaded CTA.
+// Returns the makespan, or -1 when the entries do not fit the table.
+double build_deal(const BwdParams& p, int grid, int x, BwdDealArg<2>* out) {
+    const int n = p.BHk * p.n_kv, G = p.H / p.Hk;
+    struct E {
+        double cost;
+        int code;
+    };
+    std::vector<E> es;
+    es.reserve(n + x);
+    for (int i = 0; i < n; ++i) {
+        const int steps = G * (p.n_kv - i / p.BHk);
+        if (i < x) {
+            es.push_back({steps / 2 + kDealItemCost, i | 0x8000});
+            es.push_back({steps - steps / 2 + kDealItemCost, i | 0x8000 | 0x4000});
+        } else {
+            es.push_back({steps + kDealItemCost, i});
+        }
+    }
+    if (static_cast<int>(es.size()) > kDealMax) return -1.0;
+    std::stable_sort(es.begin(), es.end(), [](const E& a, const E& b) { return a.cost > b.cost; });
+    using L = std::pair<double, int>;  // (load, CTA)
+    std::priority_queue<L, std::vector<L>, std::greater<L>> heap;
+    for (int c = 0; c < grid; ++c) heap.push({0.0, c});
+    std::vector<std::vector<uint16_t>> lists(grid);
+    double makespan = 0.0;
+    for (const E& e : es) {
+        L top = heap.top();
+        heap.pop();
+        top.first += e.cost;
+        makespan = std::max(makespan, top.first);
+        lists[top.second].push_back(static_cast<uint16_t>(e.code));
+        heap.push(top);
+    }
+    if (out != nullptr) {
+        int k = 0;
+        for (int c = 0; c < grid; ++c) {
+            out->start[c] = static_cast<uint16_t>(k);
+            for (uint16_t v : lists[c]) out->entry[k++] = v;
+        }
+        for (int c = grid; c <= kDealGrid; ++c) out->start[c] = static_cast<uint16_t>(k);
+    }
+    return makespan;
+}
+
+// Fills *out and returns true when a deal over `grid` CTAs is worth it for this
+// causal launch, against the snake order over `snake_grid` CTAs (the items, when
+// there are fewer than CTAs).
+bool bwd_deal_for(const BwdParams& p, int snake_grid, int grid, BwdDealArg<2>* out) {
+    const int n = p.BHk * p.n_kv, G = p.H / p.Hk;
+    if (!p.causal || grid > kDealGrid || n > 0x3FFF || p.split_cap < 2) return false;
+    struct Cached {
+        long long key[6];
+        bool use;
+        BwdDealArg<2> deal;
+    };
+    static std::mutex mu;
+    static std::vector<Cached> cache;  // a few shapes; the oldest is replaced
+    static size_t next = 0;
+    const long long key[6] = {p.BHk, p.n_kv, G, grid, snake_grid, p.split_cap};
+    std::lock_guard<std::mutex> lock(mu);
+    for (const Cached& c : cache)
+        if (std::equal(key, key + 6, c.key)) {
+            if (c.use) *out = c.deal;
+            return c.use;
+        }
+    std::vector<double> cost(n);
+    double total = 0.0;
+    for (int i = 0; i < n; ++i) total += cost[i] = G * (p.n_kv - i / p.BHk) + kDealItemCost;
+    const double snake = snake_makespan(cost, snake_grid), mean = total / grid;
+    int best_x = -1;
+    double best = snake;
+    for (double thr : {0.6, 0.75, 0.9, 1.0, 1.2}) {
+        int x = 0;
+        while (x < n && cost[x] > thr * mean) ++x;
+        x = std::min(x, p.split_cap / 2);
+        const double m = build_deal(p, grid, x, nullptr);
+        if (m > 0.0 && m < best) {
+            best = m;
+            best_x = x;
+        }
+    }
+    Cached c{};
+    std::copy(key, key + 6, c.key);
+    c.use = best_x >= 0 && best < 0.97 * snake;
+    if (c.use) build_deal(p, grid, best_x, &c.deal);
+    if (cache.size() < 8) {
+        cache.push_back(c);
+    } else {
+        cache[next] = c;
+        next = (next + 1) % cache.size();
+    }
+    if (c.use) *out = c.deal;
+    return c.use;
+}
+
 template <int D>
 cudaError_t launch_bwd_main_impl(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                  const CUtensorMap& tdo, const CUtensorMap& tdq, const BwdParams& p,
@@ -1519,11 +1672,14 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
     if (D == 128) {
         using T = BwdFullTraits;
         static const cudaError_t attr = cudaFuncSetAttribute(
-            bwd_main_full_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+            bwd_main_full_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
         if (attr != cudaSuccess) return attr;
         static const cudaError_t attr_split = cudaFuncSetAttribute(
-            bwd_main_full_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+            bwd_main_full_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
         if (attr_split != cudaSuccess) return attr_split;
+        static const cudaError_t attr_deal = cudaFuncSetAttribute(
+            bwd_main_full_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+        if (attr_deal != cudaSuccess) return attr_deal;
         // persistent: one CTA per SM (shared memory admits one), items in snake order
         const long long items = static_cast<long long>(p.BHk) * p.n_kv;
         long long grid = items;
@@ -1551,12 +1707,19 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
         }
         const cudaError_t dbg = dbg_set_word(p.st.word, stream);
         if (dbg != cudaSuccess) return dbg;
-        if (pp.split_parts > 1)
-            bwd_main_full_kernel<true><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
-                tq, tk, tv, tdo, pp);
-        else
-            bwd_main_full_kernel<false><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
-                tq, tk, tv, tdo, pp);
+        BwdDealArg<2> deal;
+        const int deal_grid = sms < kDealGrid ? sms : kDealGrid;
+        if (p.causal && bwd_deal_for(p, static_cast<int>(grid), deal_grid, &deal)) {
+            pp.split_parts = 2;
+            bwd_main_full_kernel<2><<<static_cast<unsigned>(deal_grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
+                tq, tk, tv, tdo, pp, deal);
+        } else if (pp.split_parts > 1) {
+            bwd_main_full_kernel<1><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
+                tq, tk, tv, tdo, pp, BwdDealArg<1>{});
+        } else {
+            bwd_main_full_kernel<0><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
+                tq, tk, tv, tdo, pp, BwdDealArg<0>{});
+        }
         return cudaGetLastError();
     }
     return cudaErrorInvalidValue;

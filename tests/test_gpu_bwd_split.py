@@ -1,4 +1,7 @@
-"""The d = 128 backward's split last round.  With G persistent CTAs and n = R G + r
+"""The d = 128 backward's split items: the last round of a launch without a mask,
+and the longest items of causal launches with grouped heads.
+
+Split last round.  With G persistent CTAs and n = R G + r
 key-tile items (0 < r, no mask), the last round's r items are dealt as
 P = G / r parts each (contiguous ranges of their query steps); every part leaves
 an fp32 dV/dK partial in the workspace and the last part to finish a 32-row slice
@@ -8,6 +11,13 @@ compare dQ, dK and dV with the fp64 oracle, block by block:
   * grouped heads, where a part's steps run across query heads of the group;
   * a ragged N, whose last key tile has rows past the sequence end.
 The split also runs at B1 H32 N8192 d128 in the workload and invariant tests.
+
+Causal grouped heads.  A key tile's item visits every query head of its group, so
+causal items run from G n_q steps down to G; when the longest reach the per-CTA
+mean, the host splits them in two and deals parts and whole items longest first
+from per-CTA lists passed to the kernel.  The causal shapes below take that path
+(one or two key/value heads, ragged N included).
+
 With 152 SMs (GB300) the shapes below split; on another SM count they may not,
 and the comparison with the oracle holds either way."""
 
@@ -23,11 +33,11 @@ from .helpers import TOL_GRAD_RELFRO, bf16_to_device, decoded, device_bf16_to_f6
 pytestmark = pytest.mark.gpu
 
 
-def _run(B, H, Hk, N, seed):
+def _run(B, H, Hk, N, seed, causal=False):
     inp = make_inputs_gqa(B, H, Hk, N, 128, seed=seed, with_grad=True)
     q, k, v, do = (bf16_to_device(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
-    o, lse = api.fwd(q, k, v, causal=False)
-    grads = api.bwd(q, k, v, o, do, lse, causal=False)
+    o, lse = api.fwd(q, k, v, causal=causal)
+    grads = api.bwd(q, k, v, o, do, lse, causal=causal)
     rc, site = api.check_device_error()
     assert rc == 0, f"device error {rc} at site {site:#x}"
     return inp, (q, k, v, o, do, lse), grads
@@ -83,3 +93,26 @@ def test_split_last_round_bnhd_layout():
     for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
         err = grad_rel_err(device_bf16_to_f64(g.permute(0, 2, 1, 3)), r)
         assert err <= TOL_GRAD_RELFRO, (name, err)
+
+
+# (B, H, Hk, N): causal, 16 / 48 / 8 items of up to 128 / 48 / 48 steps, all split
+CAUSAL_SHAPES = [(1, 8, 1, 2048), (2, 8, 2, 1536), (1, 6, 1, 1000)]
+
+
+@pytest.mark.parametrize("B,H,Hk,N", CAUSAL_SHAPES)
+def test_causal_long_items_dealt_match_oracle(B, H, Hk, N):
+    inp, _, grads = _run(B, H, Hk, N, seed=7000 + N + H, causal=True)
+    qf, kf, vf, dof = decoded(inp)
+    ref = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), True)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = device_bf16_to_f64(g)
+        assert np.all(np.isfinite(g)), name
+        err = grad_rel_err(g, r)
+        assert err <= TOL_GRAD_RELFRO, (name, err)
+
+
+def test_causal_dealt_is_deterministic():
+    _, args, first = _run(2, 8, 2, 1536, seed=8, causal=True)
+    second = api.bwd(*args, causal=True)
+    for name, a, b in zip(("dk", "dv"), first[1:], second[1:]):
+        assert np.array_equal(device_bf16_to_f64(a), device_bf16_to_f64(b)), name

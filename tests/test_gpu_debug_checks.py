@@ -111,3 +111,18 @@ def test_debug_build_split_last_round():
     refs = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), False)
     for g, r in zip((dq, dk, dv), refs):
         assert grad_rel_err(device_bf16_to_f64(g), r) <= TOL_GRAD_RELFRO
+
+
+def test_debug_build_causal_dealt():
+    """Causal, one key/value head for 8 query heads at N = 2048: 16 items of up
+    to 128 steps, each split in two and dealt from per-CTA lists."""
+    inp = make_inputs_gqa(1, 8, 1, 2048, 128, seed=92, with_grad=True)
+    with debug_library():
+        q, k, v, do = (bf16_to_device(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
+        o, lse = api.fwd(q, k, v, causal=True)
+        dq, dk, dv = api.bwd(q, k, v, o, do, lse, causal=True)
+        _assert_clean()
+    qf, kf, vf, dof = decoded(inp)
+    refs = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), True)
+    for g, r in zip((dq, dk, dv), refs):
+        assert grad_rel_err(device_bf16_to_f64(g), r) <= TOL_GRAD_RELFRO
