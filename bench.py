@@ -641,6 +641,9 @@ EXTRA_WORKLOADS = {
     "gqa_b1_h32_hk8_n8192_d128": dict(B=1, H=32, Hk=8, N=8192, d=128, causal=False),
     "gqa_causal_b2_h32_hk4_n4096_d128": dict(B=2, H=32, Hk=4, N=4096, d=128, causal=True),
     "mqa_b4_h16_hk1_n4096_d128": dict(B=4, H=16, Hk=1, N=4096, d=128, causal=False),
+    # causal with one key/value head: key-tile items of up to 16 x 32 steps for 128
+    # items, fewer than the CTAs (the backward deals the longest as two parts)
+    "mqa_causal_b4_h16_hk1_n4096_d128": dict(B=4, H=16, Hk=1, N=4096, d=128, causal=True),
     # sliding window of 1024 keys to the left (and the query itself)
     "window1024_b1_h32_n8192_d128": dict(B=1, H=32, Hk=32, N=8192, d=128, causal=False,
                                          window=(1024, 0)),
