@@ -20,8 +20,10 @@
 //   d = 128  bwd_main_full_kernel: persistent CTAs, whole 128x128 query tiles,
 //            every product 128 wide, the steps pipelined so that the
 //            exponential and dS passes overlap dP^T and dV (section 2b below).
-//            Its <true> instantiation also splits a short last round of key
-//            tiles into parts that meet in the workspace (no mask only).
+//            Its instantiation <1> also splits a short last round of key tiles
+//            into parts that meet in the workspace (no mask); <2> takes per-CTA
+//            lists built on the host, with the longest causal items in two parts
+//            (grouped heads whose longest items pass the per-CTA mean).
 //   d = 64   bwd_main_kernel<64>: one CTA per key tile, each query tile as two
 //            64-row halves with their own compute warpgroup and tensor-memory
 //            region, dQ staged in shared memory and TMA-reduced (section 2).
