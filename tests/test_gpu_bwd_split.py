@@ -116,3 +116,19 @@ def test_causal_dealt_is_deterministic():
     second = api.bwd(*args, causal=True)
     for name, a, b in zip(("dk", "dv"), first[1:], second[1:]):
         assert np.array_equal(device_bf16_to_f64(a), device_bf16_to_f64(b)), name
+
+
+def test_causal_dealt_full_size_mqa_batch0():
+    """The dealt launch at full size, B4 H16 Hk1 N4096 causal (128 items of up to
+    512 steps, the 80 longest split in two): every gradient of batch 0 (dQ of its
+    16 query heads, dK and dV of its key/value head) against the oracle, block by
+    block; the other batches' gradients finite."""
+    B, H, Hk, N = 4, 16, 1, 4096
+    inp, _, grads = _run(B, H, Hk, N, seed=4242, causal=True)
+    qf, kf, vf, dof = decoded(inp)
+    ref = oracle.backward_gqa(qf[:1], kf[:1], vf[:1], dof[:1], 1.0 / np.sqrt(128), True)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = device_bf16_to_f64(g)
+        assert np.all(np.isfinite(g)), name
+        err = grad_rel_err(g[:1], r)
+        assert err <= TOL_GRAD_RELFRO, (name, err)
