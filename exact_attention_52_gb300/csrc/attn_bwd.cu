@@ -1520,6 +1520,13 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // deal with the longest items split, for a few split thresholds; the best deal
 // is used when it ends at least 3 % sooner.  Results are cached per shape.
 constexpr double kDealItemCost = 1.5;  // per-item overhead in steps (clock stamps: ~3.4 us / 2.3 us)
+constexpr double kDealPartCost = 2.0;  // a part's fp32 partial written and summed, in steps
+// Shorter items are never dealt: with at most 16 steps the parts' partials and the
+// lost spread of the dQ reductions (a second walker per item, starting halfway up
+// its query tiles, meets the walker of the item that starts there) made B2 H4
+// N1024 and B1 H8 N2048 causal 45-50 % slower, while items of 64 steps and more
+// gained 15-38 %.
+constexpr int kDealMinLongest = 64;
 
 double snake_makespan(const std::vector<double>& cost, int grid) {
     std::vector<double> load(grid, 0.0);
@@ -1546,8 +1553,8 @@ double build_deal(const BwdParams& p, int grid, int x, BwdDealArg<2>* out) {
     for (int i = 0; i < n; ++i) {
         const int steps = G * (p.n_kv - i / p.BHk);
         if (i < x) {
-            es.push_back({steps / 2 + kDealItemCost, i | 0x8000});
-            es.push_back({steps - steps / 2 + kDealItemCost, i | 0x8000 | 0x4000});
+            es.push_back({steps / 2 + kDealItemCost + kDealPartCost, i | 0x8000});
+            es.push_back({steps - steps / 2 + kDealItemCost + kDealPartCost, i | 0x8000 | 0x4000});
         } else {
             es.push_back({steps + kDealItemCost, i});
         }
@@ -1583,7 +1590,8 @@ double build_deal(const BwdParams& p, int grid, int x, BwdDealArg<2>* out) {
 // there are fewer than CTAs).
 bool bwd_deal_for(const BwdParams& p, int snake_grid, int grid, BwdDealArg<2>* out) {
     const int n = p.BHk * p.n_kv, G = p.H / p.Hk;
-    if (!p.causal || grid > kDealGrid || n > 0x3FFF || p.split_cap < 2) return false;
+    if (!p.causal || grid > kDealGrid || n > 0x3FFF || p.split_cap < 2 || G * p.n_kv < kDealMinLongest)
+        return false;
     struct Cached {
         long long key[6];
         bool use;
