@@ -1614,8 +1614,8 @@ bool bwd_deal_for(const BwdParams& p, int snake_grid, int grid, BwdDealArg<2>* o
     int best_x = -1;
     double best = snake;
     for (double thr : {0.6, 0.75, 0.9, 1.0, 1.2}) {
-        int x = 0;
-        while (x < n && cost[x] > thr * mean) ++x;
+        int x = 0;  // items are split only with two steps or more (a part never has none)
+        while (x < n && cost[x] > thr * mean && cost[x] >= 2 + kDealItemCost) ++x;
         x = std::min(x, p.split_cap / 2);
         const double m = build_deal(p, grid, x, nullptr);
         if (m > 0.0 && m < best) {

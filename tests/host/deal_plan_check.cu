@@ -2,7 +2,9 @@
 // for causal problems of many shapes, with 152 SMs, the per-CTA lists must hold
 // every key-tile item exactly once, whole or as both of its parts, use partial
 // slots the workspace has, and fit the table.  Compiled and run by
-// tests/test_bwd_deal_plan.py; nothing is launched on a GPU.
+// tests/test_bwd_deal_plan.py; nothing is launched on a GPU.  A split item must
+// have two steps at least (each of its two parts takes half of them, and neither
+// may be empty).
 #include "attn_bwd.cu"
 
 #include <cstdio>
@@ -48,7 +50,8 @@ int main() {
                         if (v & 0x8000) {
                             const int part = (v >> 14) & 1;
                             (part ? part1 : part0)[it]++;
-                            ok = ok && 2 * it + part < p.split_cap && it < kBwdSplitCntWords / 8;
+                            const int steps = (p.H / p.Hk) * (p.n_kv - it / p.BHk);
+                            ok = ok && 2 * it + part < p.split_cap && it < kBwdSplitCntWords / 8 && steps >= 2;
                         } else {
                             ok = ok && (v & 0x4000) == 0;
                             whole[it]++;

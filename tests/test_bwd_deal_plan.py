@@ -3,8 +3,8 @@ tests/host/deal_plan_check.cu includes the backward's source, asks it for the
 per-CTA lists of causal problems of many shapes (batch, query and key/value
 heads, ragged and long sequences) on 152 SMs, and checks that every key-tile
 item appears exactly once, whole or as both of its two parts, that the lists are
-ordered and fit the table, and that parts use only the workspace's partial slots
-and counters.  A dropped or doubled item would otherwise only show as wrong
+ordered and fit the table, that parts use only the workspace's partial slots
+and counters, and that no split item has fewer than two steps.  A dropped or doubled item would otherwise only show as wrong
 gradients for the shapes the GPU tests happen to run."""
 
 import os
