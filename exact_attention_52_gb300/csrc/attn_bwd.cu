@@ -1521,11 +1521,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 // is used when it ends at least 3 % sooner.  Results are cached per shape.
 constexpr double kDealItemCost = 1.5;  // per-item overhead in steps (clock stamps: ~3.4 us / 2.3 us)
 constexpr double kDealPartCost = 2.0;  // a part's fp32 partial written and summed, in steps
-// Shorter items are never dealt: with at most 16 steps the parts' partials and the
-// lost spread of the dQ reductions (a second walker per item, starting halfway up
-// its query tiles, meets the walker of the item that starts there) made B2 H4
-// N1024 and B1 H8 N2048 causal 45-50 % slower, while items of 64 steps and more
-// gained 15-38 %.
+// Shorter items are never dealt: with items of at most 16 steps a deal made B2 H4
+// N1024 and B1 H8 N2048 causal 45-50 % slower (the parts' partials and epilogues
+// against a few steps of work), while items of 64 steps and more gained 14-39 %.
 constexpr int kDealMinLongest = 64;
 
 double snake_makespan(const std::vector<double>& cost, int grid) {
