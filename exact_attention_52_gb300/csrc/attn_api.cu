@@ -180,8 +180,9 @@ struct BwdLayout {
 };
 
 // fp32 dQ accumulator, -LSE log2 e, D; for d = 128 (split) also the counters and
-// partials of a split last round: at most min(kBwdSplitCap, items - 1) parts,
-// items <= B * H * ceil(N / 128) (a split needs more items than CTAs).
+// partials of split items: at most min(kBwdSplitCap, items * min(10, ceil(N / 128)))
+// parts, items <= B * H * ceil(N / 128) (an item is split at most ten ways, and
+// never into more parts than its steps).
 BwdLayout bwd_layout(int B, int H, int N, int d, bool split) {
     const size_t rows = static_cast<size_t>(B) * H * npad(N);
     BwdLayout L;
@@ -192,8 +193,9 @@ BwdLayout bwd_layout(int B, int H, int N, int d, bool split) {
     L.total = L.split_cnt;
     L.split_cap = 0;
     if (split && d == 128) {
-        const long long items = static_cast<long long>(B) * H * (npad(N) / kTile);
-        L.split_cap = static_cast<int>(items - 1 < kBwdSplitCap ? items - 1 : kBwdSplitCap);
+        const long long tiles = npad(N) / kTile;
+        const long long room = static_cast<long long>(B) * H * tiles * (tiles < 10 ? tiles : 10);
+        L.split_cap = static_cast<int>(room < kBwdSplitCap ? room : kBwdSplitCap);
         if (L.split_cap > 0) {
             L.split_part = L.split_cnt + round256(kBwdSplitCntWords * sizeof(unsigned));
             L.total = L.split_part + round256(static_cast<size_t>(L.split_cap) * 2 * kTile * d * sizeof(float));

@@ -1525,6 +1525,7 @@ constexpr double kDealPartCost = 2.0;  // a part's fp32 partial written and summ
 // N1024 and B1 H8 N2048 causal 45-50 % slower (the parts' partials and epilogues
 // against a few steps of work), while items of 64 steps and more gained 14-39 %.
 constexpr int kDealMinLongest = 64;
+constexpr int kSplitMinPartSteps = 16;  // steps a part of the split last round keeps at least
 
 double snake_makespan(const std::vector<double>& cost, int grid) {
     std::vector<double> load(grid, 0.0);
@@ -1698,19 +1699,24 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
         if (sms < grid) grid = sms;
         if (grid < 1) return cudaSuccess;
         // Split the last round when it would leave CTAs idle (no mask: every item
-        // has the same steps), into P = grid / r parts per item, P >= 2.
+        // has the same steps), into P = grid / r parts per item, P >= 2; with fewer
+        // items than SMs, the only round: every item in P = SMs / items parts, on
+        // P times as many CTAs.  A part keeps at least kSplitMinPartSteps steps:
+        // splitting 16-step items in two made B1 H4 N2048 19 % slower, 32-step
+        // ones (B1 H2 N4096) 7 % faster.
         BwdParams pp = p;
         pp.split_base = static_cast<int>(items);
         pp.split_parts = 1;
-        const long long rem = items % grid;
+        const long long rem = items < sms ? items : items % grid;
         const long long steps = static_cast<long long>(p.H / p.Hk) * p.n_kv;
         if (rem > 0 && p.causal == 0 && p.win_left < 0 && p.win_right < 0 && p.split_cap > 0) {
-            long long parts = grid / rem;
-            if (parts > steps) parts = steps;
+            long long parts = (items < sms ? sms : grid) / rem;
+            if (parts > steps / kSplitMinPartSteps) parts = steps / kSplitMinPartSteps;
             if (parts * rem > p.split_cap) parts = p.split_cap / rem;
             if (parts >= 2) {
                 pp.split_base = static_cast<int>(items - rem);
                 pp.split_parts = static_cast<int>(parts);
+                if (items < sms) grid = items * parts;
             }
         }
         const cudaError_t dbg = dbg_set_word(p.st.word, stream);

@@ -80,9 +80,9 @@ attn_status attn_fwd(const void* q, const void* k, const void* v, void* o, float
  * Bytes of device scratch attn_bwd needs for (B, H, N, d): an fp32 dQ
  * accumulator [B*H, Npad, d] plus two fp32 vectors [B*H, Npad] (LSE in log2
  * units and D), Npad = N rounded up to 128; for d = 128 also 5 KB of counters
- * and room for fp32 dV/dK partials of min(160, B*H*Npad/128 - 1) parts of a
- * split last round of key tiles (128 KB each; see attn_bwd).  Every region
- * starts on a 256-byte boundary.  Returns 0 for invalid sizes.
+ * and room for fp32 dV/dK partials of min(160, B*H*T*min(10, T)) parts of
+ * split key-tile items, T = Npad/128 (128 KB each; see attn_bwd).  Every
+ * region starts on a 256-byte boundary.  Returns 0 for invalid sizes.
  */
 size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
 
@@ -99,9 +99,11 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  * conversion.  dQ's summation order varies from run to run (scatter-add
  * item 52); dK and dV are deterministic.  d = 128 without a mask: the main
  * kernel's CTAs (one per SM) take key tiles in rounds; when the last round
- * has fewer key tiles than CTAs, each of them is shared by several CTAs (its
- * query tiles split into parts), whose fp32 dV/dK partials are added in the
- * workspace in part order by the last part to finish.
+ * (or the only one, with fewer key tiles than SMs) has fewer key tiles than
+ * CTAs, each of them is shared by several CTAs (its query tiles split into
+ * parts), whose fp32 dV/dK partials are added in the workspace in part order
+ * by the last part to finish.  Causal with few key/value heads: the longest
+ * key tiles are split in two the same way when that shortens the launch.
  * Source: ai.engineer item 58 (backward regenerates score tiles from saved
  * normalisation statistics); FlashAttention-3 digest section 1 (dQ-writer
  * warp and atomic accumulation); the gradient formulas are the calculus of

@@ -27,7 +27,8 @@ int main() {
                     p.n_kv = (N + 127) / 128;
                     p.causal = 1;
                     const long long items = static_cast<long long>(p.BHk) * p.n_kv;
-                    const long long room = static_cast<long long>(B) * H * p.n_kv - 1;
+                    // the workspace's room for partials (attn_bwd_workspace_bytes)
+                    const long long room = static_cast<long long>(B) * H * p.n_kv * (p.n_kv < 10 ? p.n_kv : 10);
                     p.split_cap = static_cast<int>(room < kBwdSplitCap ? room : kBwdSplitCap);
                     if (p.split_cap < 0) p.split_cap = 0;
                     const int snake_grid = static_cast<int>(items < sms ? items : sms);

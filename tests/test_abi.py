@@ -47,14 +47,16 @@ def test_status_strings(lib):
 
 def test_workspace_bytes(lib):
     # fp32 dQ accumulator over padded rows + two fp32 vectors, 256-byte rounded;
-    # d = 128 adds the counters (160 x 8 words) and fp32 dV/dK partials of a split
-    # last round: min(160, items - 1) parts of 2 x 128 x d floats, items = B*H*ceil(N/128)
+    # d = 128 adds the counters (160 x 8 words) and fp32 dV/dK partials of split
+    # items: min(160, items * min(10, tiles)) parts of 2 x 128 x d floats,
+    # tiles = ceil(N/128), items = B*H*tiles
     r256 = lambda x: (x + 255) // 256 * 256
     for B, H, N, d in ((2, 3, 200, 128), (2, 3, 200, 64), (1, 1, 128, 128), (1, 32, 8192, 128)):
         npad = (N + 127) // 128 * 128
         rows = B * H * npad
         base = r256(rows * d * 4) + 2 * r256(rows * 4)
-        cap = min(160, B * H * npad // 128 - 1) if d == 128 else 0
+        tiles = npad // 128
+        cap = min(160, B * H * tiles * min(10, tiles)) if d == 128 else 0
         split = r256(160 * 8 * 4) + r256(cap * 2 * 128 * d * 4) if cap > 0 else 0
         assert lib.attn_bwd_workspace_bytes(B, H, N, d) == base + split, (B, H, N, d)
     assert lib.attn_bwd_workspace_bytes(0, 1, 1, 64) == 0

@@ -1,5 +1,6 @@
-"""The d = 128 backward's split items: the last round of a launch without a mask,
-and the longest items of causal launches with grouped heads.
+"""The d = 128 backward's split items: the last round of a launch without a mask
+(or its only round, with fewer items than SMs), and the longest items of causal
+launches with grouped heads.
 
 Split last round.  With G persistent CTAs and n = R G + r
 key-tile items (0 < r, no mask), the last round's r items are dealt as
@@ -7,9 +8,10 @@ P = G / r parts each (contiguous ranges of their query steps); every part leaves
 an fp32 dV/dK partial in the workspace and the last part to finish a 32-row slice
 adds them up in part order.  These shapes put every kind of part on the GPU and
 compare dQ, dK and dV with the fp64 oracle, block by block:
-  * 8 query tiles per key tile and P = 8: parts of a single step;
-  * grouped heads, where a part's steps run across query heads of the group;
-  * a ragged N, whose last key tile has rows past the sequence end.
+  * grouped heads, where a part's steps run across query heads of the group and
+    may start inside one;
+  * a ragged N, whose last key tile has rows past the sequence end;
+  * fewer items than SMs, where every item is split.
 The split also runs at B1 H32 N8192 d128 in the workload and invariant tests.
 
 Causal grouped heads.  A key tile's item visits every query head of its group, so
@@ -44,12 +46,16 @@ def _run(B, H, Hk, N, seed, causal=False):
     return inp, (q, k, v, o, do, lse), grads
 
 
-# (B, H, Hk, N): items B*Hk*ceil(N/128) against 152 CTAs
+# (B, H, Hk, N): items B*Hk*ceil(N/128) against 152 CTAs; a part keeps 16 steps
+# at least (steps of an item: (H / Hk) * ceil(N/128))
 SHAPES = [
-    (2, 20, 20, 1024),   # 320 items: r = 16, P = 8 parts of one step each
-    (2, 24, 8, 2560),    # 320 items of 60 steps over 3 query heads: P = 9 parts of 6-7 steps
-    (1, 40, 40, 1000),   # 320 items, ragged last key tile: P = 8
-    (1, 20, 10, 2048),   # 160 items of 32 steps: r = 8, P = 19 parts of 1-2 steps
+    (2, 32, 8, 1280),    # 160 items of 40 steps: r = 8, P = 2 parts of 20
+    (1, 20, 10, 2048),   # 160 items of 32 steps: r = 8, P = 2 parts of 16
+    # fewer items than SMs: every item in parts, on P times as many CTAs
+    (1, 1, 1, 4096),     # 32 items of 32 steps: P = 2
+    (2, 24, 4, 1024),    # 64 items of 48 steps over 6 query heads: P = 2
+    (1, 6, 1, 1536),     # 12 items of 72 steps: P = 4 parts of 18 (parts start mid-head)
+    (1, 32, 4, 1000),    # 32 items of 64 steps, ragged last key tile: P = 4
 ]
 
 
@@ -68,7 +74,7 @@ def test_split_last_round_matches_oracle(B, H, Hk, N):
 def test_split_last_round_is_deterministic():
     """dK and dV of split items are summed in part order, whichever part ends
     last: two calls give the same bits."""
-    _, args, first = _run(2, 20, 20, 1024, seed=5)
+    _, args, first = _run(2, 24, 4, 1024, seed=5)
     second = api.bwd(*args, causal=False)
     for name, a, b in zip(("dk", "dv"), first[1:], second[1:]):
         assert np.array_equal(device_bf16_to_f64(a), device_bf16_to_f64(b)), name
@@ -77,7 +83,7 @@ def test_split_last_round_is_deterministic():
 def test_split_last_round_bnhd_layout():
     """A split last round writing dK and dV through [B, N, H, d] strides (rows of
     a key tile 8 heads apart) with grouped heads: 2 x 4 kv heads x 20 key tiles
-    = 160 items, the last 8 in 19 parts."""
+    = 160 items of 40 steps, the last 8 in 2 parts."""
     B, H, Hk, N = 2, 8, 4, 2560
     inp = make_inputs_gqa(B, H, Hk, N, 128, seed=606, with_grad=True)
 

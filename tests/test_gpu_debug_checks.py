@@ -99,8 +99,9 @@ def test_debug_build_splitkv_and_fp8():
 
 
 def test_debug_build_split_last_round():
-    """d = 128 without a mask, 160 key-tile items for 152 CTAs: the last round's
-    8 items are split into 19 parts each, whose partials meet in the workspace."""
+    """d = 128 without a mask, 160 key-tile items of 32 steps for 152 CTAs: the
+    last round's 8 items are split into 2 parts each, whose partials meet in the
+    workspace."""
     inp = make_inputs_gqa(1, 20, 10, 2048, 128, seed=91, with_grad=True)
     with debug_library():
         q, k, v, do = (bf16_to_device(x) for x in (inp.q_bits, inp.k_bits, inp.v_bits, inp.do_bits))
