@@ -80,6 +80,9 @@ def test_small_workloads_every_element(name):
     assert max_abs(device_f32_to_f64(lse), lse_ref) <= TOL_LSE_ABS
 
 
+# B1 H32 N8192: 2048 key-tile items for 152 CTAs, the last 72 (key tiles 56-63 of
+# head 30 and all of head 31) split into two parts each, so head 31's dK and dV
+# come entirely from summed partials
 @pytest.mark.parametrize("name,full_heads", [
     ("fwdbwd_causal_b2_h16_n4096_d128", [(0, 0), (0, 9), (1, 4), (1, 15)]),
     ("fwdbwd_b1_h32_n8192_d128_outlierK", [(0, 0), (0, 11), (0, 22), (0, 31)]),
