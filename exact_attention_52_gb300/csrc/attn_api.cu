@@ -272,6 +272,7 @@ attn_status fwd_run(const void* q, const Strides& qs, const void* k, const Strid
     p.o_part = split.o_part;
     p.lse_part = split.lse_part;
     p.exp2_offload = 0;
+    p.single = 0;
     p.st = dev_status(ds);
     return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
@@ -622,6 +623,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
     p.o_part = nullptr;
     p.lse_part = nullptr;
     p.exp2_offload = g_exp2_offload;
+    p.single = 0;
     p.st = dev_status(ds);
     return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK

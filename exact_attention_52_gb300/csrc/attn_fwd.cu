@@ -127,7 +127,11 @@ __global__ void __launch_bounds__(320, 1)
     const bool split_mode = prm.n_splits > 1;
     const bool lpt = prm.causal != 0;
     const int N = prm.N;
-    const int n_items = prm.BH * prm.n_pairs * prm.n_splits;
+    // Work units of a head: query-tile pairs, or single tiles when the launch has so
+    // few pairs that they would leave at least half of the SMs idle (a CTA then
+    // runs one tile's chain, and twice as many CTAs share the work).
+    const int n_units = prm.single ? (N + kTile - 1) / kTile : prm.n_pairs;
+    const int n_items = prm.BH * n_units * prm.n_splits;
     struct Item {
         int split, bh, pair, kv_lo, n_kv, b_idx, h_idx, hk_idx;
         int lo0, lo1, n0, n1;  // key-tile range [lo_g, lo_g + n_g) of query tile g
@@ -138,8 +142,10 @@ __global__ void __launch_bounds__(320, 1)
         Item w;
         const int cta = item / prm.n_splits;
         w.split = item % prm.n_splits;
-        w.bh = lpt ? cta % prm.BH : cta / prm.n_pairs;
-        w.pair = prm.n_pairs - 1 - (lpt ? cta / prm.BH : cta % prm.n_pairs);
+        w.bh = lpt ? cta % prm.BH : cta / n_units;
+        const int unit = n_units - 1 - (lpt ? cta / prm.BH : cta % n_units);
+        w.pair = prm.single ? unit >> 1 : unit;
+        const int g_only = prm.single ? unit & 1 : -1;  // the one live tile of a single item
         // Query tile g uses key tiles [lo_g, lo_g + n_g): the tiles holding
         // keys visible to some row of the tile (window i - win_left <= key <=
         // i + win_right, a negative bound meaning none), cut to the item's split.
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(320, 1)
             const int key_hi = prm.win_right < 0 ? N - 1 : min(N - 1, r1 + prm.win_right);
             const int lo = max(key_lo / kTile, w.split * prm.split_len);
             const int hi = min(key_hi / kTile, w.split * prm.split_len + prm.split_len - 1);
-            const bool live = r0 < N && key_lo <= key_hi && hi >= lo;
+            const bool live = (g_only < 0 || g == g_only) && r0 < N && key_lo <= key_hi && hi >= lo;
             if (g == 0) {
                 w.lo0 = live ? lo : 0;
                 w.n0 = live ? hi - lo + 1 : 0;
@@ -814,19 +820,26 @@ cudaError_t launch_fwd_impl(const CUtensorMap& tq, const CUtensorMap& tk, const 
     // Persistent CTAs, one per SM (shared memory admits one), each looping over
     // items in the snake order of item_at: equal items (no mask) and longest-first
     // causal items alike end within about one item of each other.
-    const long long items = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
+    FwdParams pp = p;
+    pp.single = 0;
+    long long items = static_cast<long long>(p.BH) * p.n_pairs * p.n_splits;
     long long grid = items;
     {
         int dev = 0, sms = 0;
         cudaError_t e = cudaGetDevice(&dev);
         if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
+        if (p.n_splits == 1 && 2 * items <= sms) {  // single query tiles: twice the CTAs
+            pp.single = 1;
+            items = static_cast<long long>(p.BH) * ((p.N + kTile - 1) / kTile);
+            grid = items;
+        }
         if (sms < grid) grid = sms;
     }
     if (grid < 1) return cudaSuccess;
     const cudaError_t dbg = dbg_set_word(p.st.word, stream);
     if (dbg != cudaSuccess) return dbg;
-    fwd_kernel<D, FP8, FMAEXP><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, p);
+    fwd_kernel<D, FP8, FMAEXP><<<static_cast<unsigned>(grid), 320, T::SMEM_BYTES, stream>>>(tq, tk, tv, pp);
     return cudaGetLastError();
 }
 

@@ -37,6 +37,8 @@ struct FwdParams {
     float* o_part;    // fp32 [n_splits, BH, N, D]
     float* lse_part;  // fp32 [n_splits, BH, N]; -inf where a split saw no key
     int exp2_offload; // FP8: one group of four exponentials in eight on the FMA pipe
+    int single;       // items are single query tiles (set by the launcher when pairs would
+                      // leave at least half of the SMs idle)
     DevStatus st;
 };
 
