@@ -140,3 +140,42 @@ def test_causal_dealt_full_size_mqa_batch0():
         assert np.all(np.isfinite(g)), name
         err = grad_rel_err(g[:1], r)
         assert err <= TOL_GRAD_RELFRO, (name, err)
+
+
+def _sweep_cases(n_cases, seed):
+    """Seeded shapes around the split and deal thresholds of 152 SMs, ragged N:
+    even cases without a mask (key-tile items = B * Hk * ceil(N/128) from a few
+    dozen to a few hundred, items of (H/Hk) * ceil(N/128) steps from 8 to 160),
+    odd cases causal with 8 or 16 query heads per key/value head (longest items
+    of 64 steps or more, so that the deal is considered)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out = []
+    for i in range(n_cases):
+        if i % 2 == 0:
+            B = int(rng.integers(1, 3))
+            Hk = int(rng.choice([1, 2, 4, 8]))
+            G = int(rng.choice([1, 2, 4, 8]))
+            N = int(rng.integers(300, 2561))
+            causal = False
+        else:
+            B = 1
+            Hk = int(rng.choice([1, 2]))
+            G = int(rng.choice([8, 16]))
+            N = int(rng.integers(1025, 2561))
+            causal = True
+        out.append((i, B, G * Hk, Hk, N, causal))
+    return out
+
+
+@pytest.mark.parametrize("case", _sweep_cases(16, 4077),
+                         ids=lambda c: f"s{c[0]}-B{c[1]}H{c[2]}Hk{c[3]}N{c[4]}-{'causal' if c[5] else 'full'}")
+def test_split_and_deal_sweep_matches_oracle(case):
+    i, B, H, Hk, N, causal = case
+    inp, _, grads = _run(B, H, Hk, N, seed=5000 + i, causal=causal)
+    qf, kf, vf, dof = decoded(inp)
+    ref = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), causal)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = device_bf16_to_f64(g)
+        assert np.all(np.isfinite(g)), name
+        err = grad_rel_err(g, r)
+        assert err <= TOL_GRAD_RELFRO, (name, err)
