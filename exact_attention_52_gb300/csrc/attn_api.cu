@@ -176,7 +176,7 @@ size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct BwdLayout {
     size_t dq_acc, lse2, dsum, split_cnt, split_part, total;
-    int split_cap;  // parts of a split last round the workspace holds (0: none)
+    int split_cap;  // parts of split items the workspace holds (0: none)
 };
 
 // fp32 dQ accumulator, -LSE log2 e, D; for d = 128 (split) also the counters and
