@@ -510,8 +510,9 @@ def run_ours(args):
                         causal=FP8["causal"], o=eo8, lse=else8)
 
         # The first copy-in and the last copy-out overlap no compute (about 3.5 ms
-        # together); 100 steps spread them to about 1 % of a step.
-        n_e2e = max(2, min(args.steps, 100))
+        # together); 100 steps spread them to about 1 % of a step (20 steps would
+        # leave 5 %), whatever the number of device-timed steps.
+        n_e2e = args.e2e_steps
         s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
         ev_in = [torch.cuda.Event() for _ in range(n_e2e)]
         ev_comp = [torch.cuda.Event() for _ in range(n_e2e)]
@@ -548,7 +549,8 @@ def run_ours(args):
             raise RuntimeError(f"device error {rc} at wait site {site:#x}")
         e2e_ms = a.elapsed_time(b) / n_e2e
         e2e = {"h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-               "pipelined": "inputs, compute and outputs of consecutive steps overlap on three streams"}
+               "pipelined": "inputs, compute and outputs of consecutive steps overlap on three streams",
+               "steps": n_e2e}
 
     elapsed_ms, e2e_ms = max_over_ranks([elapsed_ms, e2e["ms_per_step"] if e2e else 0.0], dist,
                                         dev)
@@ -628,7 +630,8 @@ def run_ours(args):
             "value": round(total_flops / (e2e["ms_per_step"] * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
             "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
-            "ms_per_step": round(e2e["ms_per_step"], 4), "pipelined": e2e["pipelined"]},
+            "ms_per_step": round(e2e["ms_per_step"], 4), "pipelined": e2e["pipelined"],
+            "steps": e2e["steps"]},
     }
     print(json.dumps(line), flush=True)
     if dist:
@@ -871,6 +874,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the oracle timing (used for profiling runs)")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end loop")
+    ap.add_argument("--e2e-steps", type=int, default=100,
+                    help="pipelined steps of the end-to-end loop (at least 2)")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the small-configuration lines (C1-C3) after the timed region")
     ap.add_argument("--no-live-peaks", action="store_true",
@@ -878,6 +883,7 @@ def main():
     ap.add_argument("--workload", choices=("main",) + tuple(EXTRA_WORKLOADS), default="main",
                     help="secondary workloads print their own line (not the benchmark step)")
     args = ap.parse_args()
+    args.e2e_steps = max(2, args.e2e_steps)
     if args.workload != "main" and args.impl == "ours":
         return run_extra(args)
     if args.impl == "reference":
