@@ -143,6 +143,7 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdPreParams
             p.lse2[v] = n < p.N ? -p.lse[static_cast<size_t>(bh) * p.N + n] * kLog2e : -INFINITY;
         }
     }
+    pdl_launch_dependents();  // the main kernel may start its set-up (it waits for this grid)
 }
 
 // ---------------------------------------------------------------------------
@@ -150,6 +151,7 @@ __global__ void __launch_bounds__(kAuxThreads) bwd_pre_kernel(const BwdPreParams
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(kAuxThreads) dq_convert_kernel(const DqConvertParams p) {
+    pdl_wait();  // launched as a dependent of the main kernel: its reductions must be done
     constexpr int TPR = D / 8;
     constexpr int RPP = kAuxThreads / TPR;
     constexpr int PASSES = kAuxRows / RPP;
@@ -1005,6 +1007,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // Launched as a dependent of the preprocess kernel: the set-up above overlapped
+    // its last blocks; D, -LSE log2 e and the zeroed dQ accumulator are read below.
+    pdl_wait();
 
     // Steps are counted over all of the CTA's items (g): the Q/dO stages and the
     // per-step barriers run on through item boundaries.
@@ -1507,6 +1512,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
     }
 
+    pdl_launch_dependents();  // the dQ conversion may be scheduled (it waits for this grid)
     tc_fence_before();
     __syncthreads();
     if (warp == 13) {
@@ -1668,10 +1674,19 @@ cudaError_t launch_dq_convert(const DqConvertParams& p, cudaStream_t stream) {
     if (p.Npad % kAuxRows != 0) return cudaErrorInvalidValue;
     const long long blocks = static_cast<long long>(p.BH) * (p.Npad / kAuxRows);
     if (blocks > 0x7fffffffll) return cudaErrorInvalidValue;
-    if (p.D == 64) dq_convert_kernel<64><<<static_cast<unsigned>(blocks), kAuxThreads, 0, stream>>>(p);
-    else if (p.D == 128) dq_convert_kernel<128><<<static_cast<unsigned>(blocks), kAuxThreads, 0, stream>>>(p);
-    else return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    // a programmatic dependent of the main kernel (see pdl_wait)
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kAuxThreads);
+    cfg.stream = stream;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    if (p.D == 64) return cudaLaunchKernelEx(&cfg, dq_convert_kernel<64>, p);
+    if (p.D == 128) return cudaLaunchKernelEx(&cfg, dq_convert_kernel<128>, p);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
@@ -1723,18 +1738,25 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
         if (dbg != cudaSuccess) return dbg;
         BwdDealArg<2> deal;
         const int deal_grid = sms < kDealGrid ? sms : kDealGrid;
+        // a programmatic dependent of the preprocess kernel (see pdl_wait)
+        cudaLaunchAttribute pdl;
+        pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        pdl.val.programmaticStreamSerializationAllowed = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kBwdThreads);
+        cfg.dynamicSmemBytes = T::SMEM_BYTES;
+        cfg.stream = stream;
+        cfg.attrs = &pdl;
+        cfg.numAttrs = 1;
         if (p.causal && bwd_deal_for(p, static_cast<int>(grid), deal_grid, &deal)) {
             pp.split_parts = 2;
-            bwd_main_full_kernel<2><<<static_cast<unsigned>(deal_grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
-                tq, tk, tv, tdo, pp, deal);
-        } else if (pp.split_parts > 1) {
-            bwd_main_full_kernel<1><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
-                tq, tk, tv, tdo, pp, BwdDealArg<1>{});
-        } else {
-            bwd_main_full_kernel<0><<<static_cast<unsigned>(grid), kBwdThreads, T::SMEM_BYTES, stream>>>(
-                tq, tk, tv, tdo, pp, BwdDealArg<0>{});
+            cfg.gridDim = dim3(static_cast<unsigned>(deal_grid));
+            return cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<2>, tq, tk, tv, tdo, pp, deal);
         }
-        return cudaGetLastError();
+        cfg.gridDim = dim3(static_cast<unsigned>(grid));
+        if (pp.split_parts > 1)
+            return cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<1>, tq, tk, tv, tdo, pp, BwdDealArg<1>{});
+        return cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<0>, tq, tk, tv, tdo, pp, BwdDealArg<0>{});
     }
     return cudaErrorInvalidValue;
 }
