@@ -104,6 +104,8 @@ size_t attn_bwd_workspace_bytes(int B, int H, int N, int d);
  * parts), whose fp32 dV/dK partials are added in the workspace in part order
  * by the last part to finish.  Causal with few key/value heads: the longest
  * key tiles are split in two the same way when that shortens the launch.
+ * Causal launches whose Q, dO and dQ accumulator pass 64 MiB take their key
+ * tiles in groups of heads, so that the heads in flight stay in the L2.
  * The main kernel and the conversion are launched as programmatic dependents
  * of the kernel before each (their set-up overlaps its tail; they wait for it
  * to complete before touching memory), which stream capture keeps.

@@ -4,7 +4,8 @@
 // slots the workspace has, and fit the table.  Compiled and run by
 // tests/test_bwd_deal_plan.py; nothing is launched on a GPU.  A split item must
 // have two steps at least (each of its two parts takes half of them, and neither
-// may be empty).
+// may be empty).  Deals without split items (head groups, for launches whose
+// working set passes half the L2) must occur among the shapes too.
 #include "attn_bwd.cu"
 
 #include <cstdio>
@@ -14,7 +15,7 @@ using namespace attn;
 
 int main() {
     const int sms = 152;
-    int checked = 0, dealt = 0, bad = 0;
+    int checked = 0, dealt = 0, grouped = 0, bad = 0;
     for (int B : {1, 2, 4})
         for (int H : {1, 2, 4, 6, 8, 16, 32})
             for (int Hk : {1, 2, 4, 8, 16, 32}) {
@@ -38,6 +39,7 @@ int main() {
                     if (!bwd_deal_for(p, snake_grid, grid, &d)) continue;
                     ++dealt;
                     std::vector<int> whole(items, 0), part0(items, 0), part1(items, 0);
+                    bool any_split = false;
                     bool ok = d.start[0] == 0;
                     for (int c = 0; c < grid; ++c) ok = ok && d.start[c] <= d.start[c + 1];
                     for (int c = grid; c < kDealGrid; ++c) ok = ok && d.start[c] == d.start[c + 1];
@@ -49,6 +51,7 @@ int main() {
                             break;
                         }
                         if (v & 0x8000) {
+                            any_split = true;
                             const int part = (v >> 14) & 1;
                             (part ? part1 : part0)[it]++;
                             const int steps = (p.H / p.Hk) * (p.n_kv - it / p.BHk);
@@ -61,12 +64,13 @@ int main() {
                     for (long long i = 0; ok && i < items; ++i)
                         ok = (whole[i] == 1 && part0[i] == 0 && part1[i] == 0) ||
                              (whole[i] == 0 && part0[i] == 1 && part1[i] == 1);
+                    if (!any_split) ++grouped;
                     if (!ok) {
                         ++bad;
                         std::printf("BAD B%d H%d Hk%d N%d\n", B, H, Hk, N);
                     }
                 }
             }
-    std::printf("checked %d dealt %d bad %d\n", checked, dealt, bad);
-    return bad == 0 && dealt > 0 ? 0 : 1;
+    std::printf("checked %d dealt %d grouped %d bad %d\n", checked, dealt, grouped, bad);
+    return bad == 0 && dealt > grouped && grouped > 0 ? 0 : 1;
 }

@@ -21,6 +21,11 @@ from per-CTA lists passed to the kernel (only when the longest item has at least
 64 steps).  The causal shapes below take that path (one or two key/value heads,
 ragged N included).
 
+Causal head groups.  When the launch's Q, dO and fp32 dQ accumulator pass 64 MiB
+and no item is split, the same per-CTA lists deal the items group by group of
+key/value heads (longest first within a group); the grouped shapes below take
+that path (grouped query heads and a ragged N included).
+
 With 152 SMs (GB300) the shapes below split; on another SM count they may not,
 and the comparison with the oracle holds either way."""
 
@@ -179,3 +184,40 @@ def test_split_and_deal_sweep_matches_oracle(case):
         assert np.all(np.isfinite(g)), name
         err = grad_rel_err(g, r)
         assert err <= TOL_GRAD_RELFRO, (name, err)
+
+
+def test_causal_head_groups_match_oracle():
+    """B4 H8 Hk4 N2100 causal (16 key/value heads of 17 key tiles, items of 2 to
+    34 steps, 71 MB of Q, dO and dQ accumulator): dealt in groups of key/value
+    heads; every gradient of every head against the oracle, block by block."""
+    B, H, Hk, N = 4, 8, 4, 2100
+    inp, _, grads = _run(B, H, Hk, N, seed=9100, causal=True)
+    qf, kf, vf, dof = decoded(inp)
+    ref = oracle.backward_gqa(qf, kf, vf, dof, 1.0 / np.sqrt(128), True)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        err = grad_rel_err(device_bf16_to_f64(g), r)
+        assert err <= TOL_GRAD_RELFRO, (name, err)
+
+
+def test_causal_head_groups_ragged_heads_sampled():
+    """B1 H16 N4500 causal (ragged last key tile, 74 MB): heads 0, 7 and 15 (the
+    first and last groups and one between) against the oracle, block by block;
+    every gradient finite."""
+    B, H, N = 1, 16, 4500
+    inp, _, grads = _run(B, H, H, N, seed=9200, causal=True)
+    qf, kf, vf, dof = decoded(inp)
+    heads = [0, 7, 15]
+    ref = oracle.backward_gqa(qf[:, heads], kf[:, heads], vf[:, heads], dof[:, heads],
+                              1.0 / np.sqrt(128), True)
+    for name, g, r in zip(("dq", "dk", "dv"), grads, ref):
+        g = device_bf16_to_f64(g)
+        assert np.all(np.isfinite(g)), name
+        err = grad_rel_err(g[:, heads], r)
+        assert err <= TOL_GRAD_RELFRO, (name, err)
+
+
+def test_causal_head_groups_deterministic():
+    _, args, first = _run(4, 8, 4, 2100, seed=11, causal=True)
+    second = api.bwd(*args, causal=True)
+    for name, a, b in zip(("dk", "dv"), first[1:], second[1:]):
+        assert np.array_equal(device_bf16_to_f64(a), device_bf16_to_f64(b)), name
