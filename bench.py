@@ -647,6 +647,9 @@ EXTRA_WORKLOADS = {
     # causal with one key/value head: key-tile items of up to 16 x 32 steps for 128
     # items, fewer than the CTAs (the backward deals the longest as two parts)
     "mqa_causal_b4_h16_hk1_n4096_d128": dict(B=4, H=16, Hk=1, N=4096, d=128, causal=True),
+    # causal with a large batch: 512 MB of Q, dO and fp32 dQ accumulator (the backward
+    # deals its key tiles in groups of heads so that the heads in flight stay in L2)
+    "causal_b4_h32_n4096_d128": dict(B=4, H=32, Hk=32, N=4096, d=128, causal=True),
     # sliding window of 1024 keys to the left (and the query itself)
     "window1024_b1_h32_n8192_d128": dict(B=1, H=32, Hk=32, N=8192, d=128, causal=False,
                                          window=(1024, 0)),
