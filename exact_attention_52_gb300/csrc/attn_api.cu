@@ -130,6 +130,15 @@ bool make_map_acc(CUtensorMap* m, const float* base, int d, int Npad, int BH, in
 
 bool aligned16(const void* p) { return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every row of a bf16 tensor (base + element strides s) starts on a 32-byte
+// boundary: the epilogues then write rows with 32-byte stores.
+int rows_v8(const void* base, const Strides& s) {
+    return (reinterpret_cast<uintptr_t>(base) & 31u) == 0 && (s.b * 2) % 32 == 0 && (s.h * 2) % 32 == 0 &&
+                   (s.n * 2) % 32 == 0
+               ? 1
+               : 0;
+}
+
 Strides dense(int heads, int N, int d) {
     Strides s;
     s.n = d;
@@ -273,6 +282,7 @@ attn_status fwd_run(const void* q, const Strides& qs, const void* k, const Strid
     p.lse_part = split.lse_part;
     p.exp2_offload = 0;
     p.single = 0;
+    p.o_v8 = rows_v8(o, os);
     p.st = dev_status(ds);
     return launch_fwd_bf16(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK
@@ -405,6 +415,7 @@ attn_status bwd_main_run(const void* q, const Strides& qs, const void* k, const 
     bp.split_cap = c.split_cap;
     bp.split_part = c.split_part;
     bp.split_cnt = c.split_cnt;
+    bp.dkv_v8 = rows_v8(dk, dks) && rows_v8(dv, dvs);
     bp.st = dev_status(c.ds);
     return launch_bwd_main(d, tq, tk, tv, tdo, tdq, bp, reinterpret_cast<cudaStream_t>(stream)) ==
                    cudaSuccess
@@ -624,6 +635,7 @@ attn_status attn_fwd_fp8(const void* q8, const void* k8, const void* v8, float s
     p.lse_part = nullptr;
     p.exp2_offload = g_exp2_offload;
     p.single = 0;
+    p.o_v8 = rows_v8(o, st);
     p.st = dev_status(ds);
     return launch_fwd_fp8(d, tq, tk, tv, p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? ATTN_OK

@@ -20,10 +20,12 @@
 //   d = 128  bwd_main_full_kernel: persistent CTAs, whole 128x128 query tiles,
 //            every product 128 wide, the steps pipelined so that the
 //            exponential and dS passes overlap dP^T and dV (section 2b below).
-//            Its instantiation <1> also splits a short last round of key tiles
-//            into parts that meet in the workspace (no mask); <2> takes per-CTA
-//            lists built on the host, with the longest causal items in two parts
-//            (grouped heads whose longest items pass the per-CTA mean).
+//            Its instantiation <1, *> also splits a short last round of key
+//            tiles into parts that meet in the workspace (no mask); <2, *> takes
+//            per-CTA lists built on the host, with the longest causal items in
+//            two parts (grouped heads whose longest items pass the per-CTA mean)
+//            or causal items in groups of heads; <*, true> writes dK and dV rows
+//            with 32-byte stores.
 //   d = 64   bwd_main_kernel<64>: one CTA per key tile, each query tile as two
 //            64-row halves with their own compute warpgroup and tensor-memory
 //            region, dQ staged in shared memory and TMA-reduced (section 2).
@@ -905,8 +907,10 @@ __device__ __forceinline__ uint2 split3_half_bf16(float v) {
 constexpr unsigned kDqPauseNs = 60;
 
 // MODE 0: items dealt in snake order; 1: the same with a split last round; 2: the
-// per-CTA lists of a BwdDeal (causal launches with long items).
-template <int MODE>
+// per-CTA lists of a BwdDeal (causal launches with long items).  V8: every dK and
+// dV row starts on a 32-byte boundary (32-byte stores in the epilogue; a runtime
+// choice between the two store widths measured 1-2 % slower than either alone).
+template <int MODE, bool V8>
 __global__ void __launch_bounds__(kBwdThreads, 1)
     bwd_main_full_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
@@ -1441,12 +1445,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 16; ++e)
                     pk[e] = empty ? 0u : pack_bf16x2(u2f(o[2 * e]) * f, u2f(o[2 * e + 1]) * f);
-                if (row_ok) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        st_global_v4(dst + c * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
-                                     pk[4 * v + 3]);
-                }
+                if (row_ok) st_global_row64<V8>(dst + c * 64, pk);
             }
         }
         ++k;
@@ -1725,15 +1724,19 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
     if (D == 64) return launch_bwd_main_impl<64>(tq, tk, tv, tdo, tdq, p, stream);
     if (D == 128) {
         using T = BwdFullTraits;
-        static const cudaError_t attr = cudaFuncSetAttribute(
-            bwd_main_full_kernel<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+        static const cudaError_t attr = [] {
+            cudaError_t e = cudaSuccess;
+            for (const void* fn : {reinterpret_cast<const void*>(bwd_main_full_kernel<0, false>),
+                                   reinterpret_cast<const void*>(bwd_main_full_kernel<1, false>),
+                                   reinterpret_cast<const void*>(bwd_main_full_kernel<2, false>),
+                                   reinterpret_cast<const void*>(bwd_main_full_kernel<0, true>),
+                                   reinterpret_cast<const void*>(bwd_main_full_kernel<1, true>),
+                                   reinterpret_cast<const void*>(bwd_main_full_kernel<2, true>)})
+                if (e == cudaSuccess)
+                    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
+            return e;
+        }();
         if (attr != cudaSuccess) return attr;
-        static const cudaError_t attr_split = cudaFuncSetAttribute(
-            bwd_main_full_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-        if (attr_split != cudaSuccess) return attr_split;
-        static const cudaError_t attr_deal = cudaFuncSetAttribute(
-            bwd_main_full_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, T::SMEM_BYTES);
-        if (attr_deal != cudaSuccess) return attr_deal;
         // persistent: one CTA per SM (shared memory admits one), items in snake order
         const long long items = static_cast<long long>(p.BHk) * p.n_kv;
         long long grid = items;
@@ -1778,15 +1781,20 @@ cudaError_t launch_bwd_main(int D, const CUtensorMap& tq, const CUtensorMap& tk,
         cfg.stream = stream;
         cfg.attrs = &pdl;
         cfg.numAttrs = 1;
+        const bool v8 = p.dkv_v8 != 0;
         if (p.causal && bwd_deal_for(p, static_cast<int>(grid), deal_grid, &deal)) {
             pp.split_parts = 2;
             cfg.gridDim = dim3(static_cast<unsigned>(deal_grid));
-            return cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<2>, tq, tk, tv, tdo, pp, deal);
+            return v8 ? cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<2, true>, tq, tk, tv, tdo, pp, deal)
+                      : cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<2, false>, tq, tk, tv, tdo, pp, deal);
         }
         cfg.gridDim = dim3(static_cast<unsigned>(grid));
         if (pp.split_parts > 1)
-            return cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<1>, tq, tk, tv, tdo, pp, BwdDealArg<1>{});
-        return cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<0>, tq, tk, tv, tdo, pp, BwdDealArg<0>{});
+            return v8 ? cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<1, true>, tq, tk, tv, tdo, pp, BwdDealArg<1>{})
+                      : cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<1, false>, tq, tk, tv, tdo, pp,
+                                           BwdDealArg<1>{});
+        return v8 ? cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<0, true>, tq, tk, tv, tdo, pp, BwdDealArg<0>{})
+                  : cudaLaunchKernelEx(&cfg, bwd_main_full_kernel<0, false>, tq, tk, tv, tdo, pp, BwdDealArg<0>{});
     }
     return cudaErrorInvalidValue;
 }

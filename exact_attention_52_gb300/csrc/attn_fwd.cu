@@ -739,22 +739,25 @@ __global__ void __launch_bounds__(320, 1)
             const float inv_l = l_norm > 0.f ? prm.out_scale / l_norm : 0.f;
             uint8_t* orow = static_cast<uint8_t*>(prm.o) +
                             (b_idx * prm.os.b + h_idx * prm.os.h + (row_ok ? q_row : 0) * prm.os.n) * 2;
+            // one copy of the loop per store width, so that each keeps its own
+            // register layout
+            auto write_rows = [&](auto v8_tag) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-                uint32_t o[32];
-                tmem_ld32(tO + 32 * c, o);
-                tmem_ld_wait(o);
-                uint32_t pk[16];
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    tmem_ld32(tO + 32 * c, o);
+                    tmem_ld_wait(o);
+                    uint32_t pk[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
-                if (row_ok) {
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        st_global_v4(orow + c * 64 + v * 16, pk[4 * v], pk[4 * v + 1], pk[4 * v + 2],
-                                     pk[4 * v + 3]);
+                    for (int i = 0; i < 16; ++i)
+                        pk[i] = pack_bf16x2(u2f(o[2 * i]) * inv_l, u2f(o[2 * i + 1]) * inv_l);
+                    if (row_ok) st_global_row64<decltype(v8_tag)::value>(orow + c * 64, pk);
                 }
-            }
+            };
+            if (prm.o_v8)
+                write_rows(std::true_type{});
+            else
+                write_rows(std::false_type{});
             if (row_ok)
                 prm.lse[static_cast<size_t>(bh) * N + q_row] =
                     l_sum > 0.f ? (m_used + log2f(l_sum)) * kLn2 : INFINITY;

@@ -39,6 +39,7 @@ struct FwdParams {
     int exp2_offload; // FP8: one group of four exponentials in eight on the FMA pipe
     int single;       // items are single query tiles (set by the launcher when pairs would
                       // leave at least half of the SMs idle)
+    int o_v8;         // every O row starts on a 32-byte boundary: 32-byte stores
     DevStatus st;
 };
 
@@ -98,6 +99,7 @@ struct BwdParams {
     int split_cap;        // parts the workspace has room for (0: no split possible)
     float* split_part;    // fp32 [part][dV, dK][128 rows][D]
     unsigned* split_cnt;  // kBwdSplitCntWords counters, zero at launch
+    int dkv_v8;           // every dK and dV row starts on a 32-byte boundary: 32-byte stores
     DevStatus st;
 };
 

@@ -631,4 +631,26 @@ __device__ __forceinline__ void st_global_v4(void* gaddr, uint32_t a, uint32_t b
                  : "memory");
 }
 
+// 32-byte store (sm_100+); gaddr must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* gaddr, const uint32_t* w) {
+    asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(gaddr), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// 64 bytes of one row (16 words): two 32-byte stores (rows 32-byte aligned) or
+// four 16-byte ones.  A row per lane leaves a warp instruction with 32 separate
+// pieces; whole 32-byte sectors halve the pieces, which at a backward item's end
+// hold up the next item's loads and first products.
+template <bool V8>
+__device__ __forceinline__ void st_global_row64(uint8_t* gaddr, const uint32_t* w) {
+    if constexpr (V8) {
+        st_global_v8(gaddr, w);
+        st_global_v8(gaddr + 32, w + 8);
+    } else {
+#pragma unroll
+        for (int v = 0; v < 4; ++v) st_global_v4(gaddr + 16 * v, w[4 * v], w[4 * v + 1], w[4 * v + 2], w[4 * v + 3]);
+    }
+}
+
 }  // namespace attn

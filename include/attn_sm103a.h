@@ -22,6 +22,9 @@
  *    keys are equal (N).  d is 64 or 128 (FP8: 128).
  *  - Pointers are DEVICE pointers, 16-byte aligned, owned by the caller; the
  *    library allocates nothing and keeps no pointer after a call returns.
+ *    Outputs whose rows all start on a 32-byte boundary (O of the forward, dK
+ *    and dV of the backward) are written with 32-byte stores, others with
+ *    16-byte ones; the results are the same bits.
  *  - Work is enqueued asynchronously on `stream` (0 = legacy default stream);
  *    nothing synchronises.  Outputs are valid once the stream reaches that
  *    point.
