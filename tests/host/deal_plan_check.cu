@@ -5,7 +5,8 @@
 // tests/test_bwd_deal_plan.py; nothing is launched on a GPU.  A split item must
 // have two steps at least (each of its two parts takes half of them, and neither
 // may be empty).  Deals without split items (head groups, for launches whose
-// working set passes half the L2) must occur among the shapes too.
+// working set passes half the L2) must occur among the shapes too, and their
+// lists must run group by group, longest first within a group.
 #include "attn_bwd.cu"
 
 #include <cstdio>
@@ -64,7 +65,25 @@ int main() {
                     for (long long i = 0; ok && i < items; ++i)
                         ok = (whole[i] == 1 && part0[i] == 0 && part1[i] == 0) ||
                              (whole[i] == 0 && part0[i] == 1 && part1[i] == 1);
-                    if (!any_split) ++grouped;
+                    if (ok && !any_split) {
+                        // a deal without split items runs group by group: some power-of-two
+                        // group size gs < BHk orders every CTA's list by group (key/value head
+                        // / gs), longest first within a group
+                        ++grouped;
+                        bool found = false;
+                        for (int gs = 1; gs < p.BHk && !found; gs *= 2) {
+                            bool sorted = true;
+                            for (int c = 0; c < grid && sorted; ++c)
+                                for (int e = d.start[c] + 1; e < d.start[c + 1] && sorted; ++e) {
+                                    const int a = d.entry[e - 1], b = d.entry[e];
+                                    const int ga = (a % p.BHk) / gs, gb = (b % p.BHk) / gs;
+                                    // items are numbered longest first: a / BHk is the length rank
+                                    sorted = ga < gb || (ga == gb && a / p.BHk <= b / p.BHk);
+                                }
+                            found = sorted;
+                        }
+                        ok = found;
+                    }
                     if (!ok) {
                         ++bad;
                         std::printf("BAD B%d H%d Hk%d N%d\n", B, H, Hk, N);
